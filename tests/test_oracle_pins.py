@@ -1,0 +1,265 @@
+"""Pins of the CPU oracle to facts fixed outside it (no GPU needed).
+
+Each test checks the oracle against something other than itself: values the
+pages print, closed forms, brute force over every possible 2:4 mask, library
+routines (numpy / torch) for the pieces that reduce to them, and invariants.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import st24_inputs as inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return inputs.raw(t.contiguous()).numpy()
+
+
+# --------------------------------------------------------------- decoding pins
+
+def test_decode_matches_torch_for_every_code():
+    # Every fp16/bf16 bit pattern and every e4m3 code decodes to torch's own value.
+    all16 = torch.arange(-32768, 32768, dtype=torch.int32).to(torch.int16)
+    for name, tdt in (("f16", torch.float16), ("bf16", torch.bfloat16)):
+        ref = all16.view(tdt).to(torch.float64).numpy()
+        got = oracle.decode(name, all16.numpy())
+        same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+        assert same.all(), name
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.decode("e4m3", codes.numpy())
+    assert ((got == ref) | (np.isnan(got) & np.isnan(ref))).all()
+    assert got[0x7E] == 448.0 and np.isnan(got[0x7F]) and got[1] == 2.0 ** -9
+    s8 = np.arange(-128, 128, dtype=np.int8)
+    assert (oracle.decode("s8", s8) == s8.astype(np.float64)).all()
+
+
+# ----------------------------------------------------------- worked example pin
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32", "e4m3", "s8"])
+def test_worked_example(dt):
+    g = load("worked_example.json")
+    # w0..w7 realised so that w0, w3 lead group 0 and w5, w6 lead group 1.
+    w = torch.tensor([[4.0, -1.0, 0.5, -3.0, 0.25, 2.0, -5.0, 1.0]])
+    W = w.to(inputs.TORCH_DTYPE[dt])
+    pruned, mask, values, meta = oracle.prune_compress(dt, bits(W))
+    kept = [k for k in range(g["dense_len"]) if mask[0, k]]
+    assert kept == g["kept"]
+    dense = oracle.decode(dt, bits(W))[0]
+    pr = oracle.decode(dt, pruned)[0]
+    for k in range(8):
+        assert pr[k] == (dense[k] if k in g["kept"] else 0.0)
+    assert list(oracle.decode(dt, values)[0]) == [dense[k] for k in g["values"]]
+    idx = [[(meta[0, gi // 2] >> (4 * (gi % 2) + 2 * j)) & 3 for j in range(2)] for gi in range(2)]
+    assert idx == g["indices"]
+    # 2 bits per index, 4 bits per group: one metadata byte for these 2 groups.
+    assert meta.shape[1] * 8 == 2 * g["bits_per_group"]
+
+
+# ------------------------------------------------------- listing's printed output
+
+def test_listing_printed_output():
+    g = load("listing_output.json")
+    torch.manual_seed(g["seed"])
+    W = torch.randn(g["rows"], g["cols"])
+    pruned, mask, values, meta = oracle.prune_compress("f32", bits(W))
+    Wp = torch.from_numpy(oracle.decode("f32", pruned))
+    p = g["printed"]
+    assert f"{(Wp == 0).double().mean().item():.1%}" == p["sparsity"]
+    groups = (Wp != 0).reshape(g["rows"], g["cols"] // 4, 4).sum(-1)
+    assert str(bool((groups == 2).all().item())) == p["all groups have exactly 2 nonzeros"]
+    # Byte accounting at 2 bytes per value (the page's FP16 accounting).
+    M, K = g["rows"], g["cols"]
+    dense_bytes = M * K * 2
+    sparse_bytes = oracle.values_bytes("f16", M, K) + oracle.meta_bytes(M, K)
+    assert f"{dense_bytes / 1024:.1f} KB" == p["dense"]
+    assert f"{sparse_bytes / 1024:.1f} KB" == p["sparse"]
+    assert f"{sparse_bytes / dense_bytes:.1%}" == p["sparse_fraction_of_dense"]
+    # The compressed arrays have exactly those sizes.
+    assert values.size * 2 + meta.size == sparse_bytes
+
+
+def test_storage_overhead_closed_form():
+    g = load("storage_overhead.json")
+    M, K = 64, 1024
+    for b, frac in g["metadata_fraction_of_dense"].items():
+        dense_bits = M * K * int(b)
+        assert oracle.meta_bytes(M, K) * 8 / dense_bits == frac
+    f16 = (oracle.values_bytes("f16", M, K) + oracle.meta_bytes(M, K)) / (M * K * 2)
+    assert f"{f16:.0%}" == g["fp16_compressed_fraction_of_dense_as_printed"]
+    assert oracle.values_bytes("e4m3", M, K) == M * K // 2
+    assert oracle.meta_row_bytes(12) == 2 and oracle.meta_row_bytes(8) == 1
+
+
+# ------------------------------------------------------------ brute-force pins
+
+def brute_force_pair(mags):
+    """All 6 ways to keep 2 of 4: the largest retained magnitude, earliest pair on a tie."""
+    best, best_sum = None, None
+    for pair in itertools.combinations(range(4), 2):   # lexicographic order
+        s = sum(mags[i] for i in pair)
+        if best_sum is None or s > best_sum:
+            best, best_sum = pair, s
+    return best
+
+
+def tie_heavy(dt, M, K, seed):
+    """Inputs with many equal magnitudes, zeros and sign flips."""
+    g = torch.Generator().manual_seed(seed)
+    if dt == "s8":
+        return torch.randint(-4, 5, (M, K), generator=g).to(torch.int8)
+    vals = torch.tensor([0.0, -0.0, 0.5, -0.5, 1.0, -1.0, 2.0, -2.0, 0.25])
+    pick = torch.randint(0, len(vals), (M, K), generator=g)
+    return vals[pick].to(inputs.TORCH_DTYPE[dt])
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3", "s8", "f32"])
+@pytest.mark.parametrize("kind", ["ties", "random"])
+def test_bruteforce_all_masks(dt, kind):
+    M, K = 48, 64
+    if kind == "ties":
+        W = tie_heavy(dt, M, K, seed=3)
+    else:
+        W = inputs.draw(dt, (M, K), 1.0, inputs.generator(11))
+    _, mask, values, meta = oracle.prune_compress(dt, bits(W))
+    mags = np.abs(oracle.decode(dt, bits(W)))
+    for m in range(M):
+        for gi in range(K // 4):
+            pair = brute_force_pair(list(mags[m, 4 * gi:4 * gi + 4]))
+            got = tuple(k for k in range(4) if mask[m, 4 * gi + k])
+            assert got == pair, (m, gi, mags[m, 4 * gi:4 * gi + 4])
+            nib = (meta[m, gi // 2] >> (4 * (gi % 2))) & 0xF
+            assert (nib & 3, nib >> 2) == pair
+
+
+def test_special_groups():
+    # All-zero group keeps slots (0, 1); equal magnitudes keep the two earliest;
+    # -0 ties +0; int8 -128 outranks 127; a NaN is kept.
+    cases = [
+        ("bf16", [0.0, 0.0, 0.0, 0.0], (0, 1)),
+        ("bf16", [1.0, -1.0, 1.0, -1.0], (0, 1)),
+        ("bf16", [-0.0, 0.0, 0.0, 3.0], (0, 3)),
+        ("f16", [0.5, 2.0, -2.0, 2.0], (1, 2)),
+        ("bf16", [1.0, float("nan"), 7.0, 2.0], (1, 2)),
+        ("bf16", [float("inf"), 1.0, float("nan"), 2.0], (0, 2)),
+    ]
+    for dt, row, want in cases:
+        W = torch.tensor([row]).to(inputs.TORCH_DTYPE[dt])
+        _, mask, _, meta = oracle.prune_compress(dt, bits(W))
+        assert tuple(k for k in range(4) if mask[0, k]) == want, row
+        assert (meta[0, 0] & 3, (meta[0, 0] >> 2) & 3) == want
+    W = torch.tensor([[-128, 127, 5, -127]], dtype=torch.int8)
+    _, mask, _, _ = oracle.prune_compress("s8", W.numpy())
+    assert tuple(k for k in range(4) if mask[0, k]) == (0, 1)
+
+
+def test_k_not_multiple_of_4_rejected():
+    with pytest.raises(ValueError):
+        oracle.prune_compress("bf16", np.zeros((2, 6), np.uint16))
+
+
+# ------------------------------------------------------------------ round trip
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3", "s8"])
+@pytest.mark.parametrize("K", [4, 12, 256, 1000])
+def test_decompress_of_compress_is_prune(dt, K):
+    W = inputs.draw(dt, (37, K), 0.02 if dt == "e4m3" else 1.0, inputs.generator(K))
+    pruned, mask, values, meta = oracle.prune_compress(dt, bits(W))
+    back = oracle.decompress(dt, values, meta, K)
+    assert np.array_equal(back.view(np.uint8), pruned.view(np.uint8))
+    # at most 2 non-zeros per group; exactly 2 kept slots, indices ascending
+    nz = (oracle.decode(dt, pruned) != 0).reshape(37, K // 4, 4).sum(-1)
+    assert nz.max() <= 2
+    assert (mask.reshape(37, K // 4, 4).sum(-1) == 2).all()
+    nib = np.stack([meta & 0xF, meta >> 4], -1).reshape(37, -1)[:, :K // 4]
+    assert ((nib & 3) < (nib >> 2)).all()
+
+
+def test_exactly_two_nonzeros_on_gaussian_inputs():
+    # fp16/bf16 Gaussian inputs have no zeros, so each group keeps exactly 2 non-zeros.
+    for dt in ("f16", "bf16"):
+        W = inputs.draw(dt, (64, 512), 0.02, inputs.generator(5))
+        pruned, *_ = oracle.prune_compress(dt, bits(W))
+        nz = (oracle.decode(dt, pruned) != 0).reshape(64, 128, 4).sum(-1)
+        assert (nz == 2).all()
+
+
+def test_decompress_rejects_invalid_metadata():
+    values = np.zeros((1, 2), np.uint16)
+    meta = np.array([[0x05]], np.uint8)   # indices (1, 1): not a valid pair
+    with pytest.raises(ValueError):
+        oracle.decompress("bf16", values, meta, 4)
+
+
+# --------------------------------------------------------------------- products
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3", "s8"])
+def test_sparse_product_equals_dense_product_of_pruned(dt):
+    M, N, K = 40, 24, 96
+    case = inputs.spmm_case(dt, "f32", M, N, K, a_std=0.5, seed=7)
+    pruned, _, values, meta = oracle.prune_compress(dt, bits(case.A))
+    Xb = bits(case.X)
+    sp, sp_acc = oracle.spmm(dt, "f32", values, meta, Xb, K)
+    de, de_acc = oracle.gemm_dense(dt, "f32", pruned, Xb)
+    assert np.array_equal(sp, de)              # same order, exact zeros added: identical
+    assert np.array_equal(sp_acc, de_acc)
+    # Against a library matmul of the decoded pruned matrix.
+    Ad = oracle.decode(dt, pruned)
+    Bd = oracle.decode(dt, Xb)
+    ref = Bd @ Ad.T                            # [N, M]
+    if dt == "s8":
+        iref = Xb.astype(np.int64) @ pruned.astype(np.int64).T
+        assert np.array_equal(sp_acc, iref)
+        assert np.array_equal(sp, iref.astype(np.float64))
+    else:
+        assert np.allclose(sp, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def test_epilogue_alpha_beta_scale():
+    M, N, K = 16, 8, 32
+    case = inputs.spmm_case("bf16", "bf16", M, N, K, alpha=0.75, beta=-1.5, with_scale=True, seed=2)
+    _, _, values, meta = oracle.prune_compress("bf16", bits(case.A))
+    acc, _ = oracle.spmm("bf16", "f32", values, meta, bits(case.X), K)
+    out, _ = oracle.spmm("bf16", "bf16", values, meta, bits(case.X), K, alpha=0.75, beta=-1.5,
+                         C_in=bits(case.C_in), scale=case.scale.numpy())
+    cin = case.C_in.to(torch.float64).numpy()
+    want = 0.75 * case.scale.numpy().astype(np.float64)[None, :] * acc - 1.5 * cin
+    assert np.allclose(out, want, rtol=1e-15, atol=0)
+    # beta == 0: C_in is not read (NaNs there do not matter).
+    nan_c = np.full((N, M), 0x7FC0, np.uint16)
+    out0, _ = oracle.spmm("bf16", "bf16", values, meta, bits(case.X), K, beta=0.0, C_in=nan_c)
+    assert np.isfinite(out0).all()
+
+
+def test_sampled_equals_full():
+    M, N, K = 64, 16, 128
+    case = inputs.spmm_case("e4m3", "bf16", M, N, K, a_std=0.02, seed=4)
+    _, _, values, meta = oracle.prune_compress("e4m3", bits(case.A))
+    full, _ = oracle.spmm("e4m3", "bf16", values, meta, bits(case.X), K)
+    rng = np.random.default_rng(0)
+    rows, cols = rng.integers(0, M, 50), rng.integers(0, N, 50)
+    samp, _ = oracle.spmm_sampled("e4m3", "bf16", values, meta, bits(case.X), K, rows, cols)
+    assert np.array_equal(samp, full[cols, rows])
+
+
+def test_threads_do_not_change_results():
+    M, N, K = 33, 9, 64
+    case = inputs.spmm_case("f16", "f32", M, N, K, seed=9)
+    _, _, values, meta = oracle.prune_compress("f16", bits(case.A))
+    a, _ = oracle.spmm("f16", "f32", values, meta, bits(case.X), K, nthreads=1)
+    b, _ = oracle.spmm("f16", "f32", values, meta, bits(case.X), K, nthreads=5)
+    assert np.array_equal(a, b)
+    assert math.isfinite(float(a.sum()))
