@@ -1,0 +1,432 @@
+"""Benchmark of the 2:4 sparse hot path on one GB300: prune + compress of the
+weights, then the sparse x dense product for a batch of activations.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl {st24,reference}]
+
+One step = prune_compress of every weight of the workload, then st24_spmm of
+every weight with every activation width of the workload.  Inputs are seeded
+synthetic tensors (st24_inputs).  The timed region is K steps replayed as CUDA
+graphs on one stream, bracketed by a barrier and a synchronize.  Prints one JSON
+line.  ``--impl reference`` times the CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import st24_inputs as inputs  # noqa: E402
+
+METRIC = "2:4 SpMM TFLOP/s and % of sparse tensor peak / HBM roofline on 1 GB300"
+UNIT = "TFLOP/s"
+
+# Workloads: (name, element type, output type, weight shapes [(M, K)], activation widths, layers,
+#             weight std, beta, per-row scale)
+WORKLOADS = {
+    "decode_bf16": dict(ab="bf16", c="bf16", shapes=[(4096, 4096)], Ns=list(inputs.DECODE_NS), layers=16,
+                        a_std=0.02, beta=0.0, scale=False,
+                        desc="decode-shaped bf16 2:4 SpMM: 16 distinct 4096x4096 weights N(0,0.02), "
+                             "activations N(0,1) for N in {1,8,16,32}, bf16 out"),
+    "prefill_bf16": dict(ab="bf16", c="bf16", shapes=list(inputs.PREFILL_SHAPES), Ns=[4096], layers=1,
+                         a_std=0.02, beta=1.0, scale=False,
+                         desc="prefill-shaped bf16 2:4 SpMM: 11008x4096 and 4096x11008 weights, N=4096, "
+                              "beta=1 with C N(0,1), bf16 out"),
+    "int8": dict(ab="s8", c="bf16", shapes=[(8192, 8192)], Ns=list(inputs.INT8_NS), layers=1, a_std=1.0,
+                 beta=0.0, scale=True,
+                 desc="int8 2:4 SpMM: 8192x8192 weights uniform [-127,127], N in {16,2048}, int32 accumulate, "
+                      "per-row fp32 scale, bf16 out"),
+    "fp8": dict(ab="e4m3", c="bf16", shapes=[(28672, 8192)], Ns=list(inputs.FP8_NS), layers=1, a_std=0.02,
+                beta=0.0, scale=False,
+                desc="fp8-e4m3 2:4 SpMM: 28672x8192 weights N(0,0.02), N in {1,64,512,4096,8192}, bf16 out"),
+}
+
+
+def flops_per_step(w):
+    return sum(2.0 * M * K * N for (M, K) in w["shapes"] for N in w["Ns"]) * w["layers"]
+
+
+def spmm_bytes(w):
+    """Algorithmic HBM bytes of all SpMM launches of one step (compressed A, B, C, scale)."""
+    es = inputs.ELEM_SIZE[w["ab"]]
+    cs = inputs.ELEM_SIZE[w["c"]]
+    total = 0
+    for (M, K) in w["shapes"]:
+        for N in w["Ns"]:
+            b = M * K // 2 * es + M * K // 8 + K * N * es + M * N * cs * (2 if w["beta"] else 1)
+            if w["scale"]:
+                b += 4 * M
+            total += b
+    return total * w["layers"]
+
+
+def prune_bytes(w):
+    es = inputs.ELEM_SIZE[w["ab"]]
+    return sum(M * K * es + M * K // 2 * es + M * K // 8 for (M, K) in w["shapes"]) * w["layers"]
+
+
+def n_spmm(w):
+    return len(w["shapes"]) * len(w["Ns"]) * w["layers"]
+
+
+def n_prune(w):
+    return len(w["shapes"]) * w["layers"]
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- the GPU arm
+def build_workload(w, dev, seed=0):
+    """Weights, activations and outputs of one workload, resident on `dev`."""
+    import structured_sparse_gemm_gb300 as st
+
+    layers = []
+    for li in range(w["layers"]):
+        for si, (M, K) in enumerate(w["shapes"]):
+            g = inputs.generator(seed + 1000 * li + si)
+            A = inputs.draw(w["ab"], (M, K), w["a_std"], g).to(dev)
+            values = torch.empty((M, K // 2), dtype=A.dtype, device=dev)
+            meta = torch.empty((M, K // 8), dtype=torch.uint8, device=dev)
+            scale = inputs.row_scale(M, g).to(dev) if w["scale"] else None
+            acts = []
+            for N in w["Ns"]:
+                X = inputs.draw(w["ab"], (N, K), 1.0, g).to(dev)
+                Y = inputs.draw(w["c"], (N, M), 1.0, g).to(dev) if w["beta"] else \
+                    torch.empty((N, M), dtype=inputs.TORCH_DTYPE[w["c"]], device=dev)
+                ws_bytes = st.st24_spmm_workspace_bytes(w["ab"], w["c"], M, N, K)
+                ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
+                acts.append((X, Y, ws))
+            layers.append(dict(A=A, values=values, meta=meta, scale=scale, acts=acts, M=M, K=K))
+    return layers
+
+
+def prune_phase(layers, stream=None):
+    import structured_sparse_gemm_gb300 as st
+    for L in layers:
+        st.st24_prune_compress(L["A"], L["values"], L["meta"], stream=stream)
+
+
+def spmm_phase(layers, w, stream=None):
+    import structured_sparse_gemm_gb300 as st
+    for ni in range(len(w["Ns"])):
+        for L in layers:
+            X, Y, ws = L["acts"][ni]
+            st.st24_spmm(L["values"], L["meta"], X, Y, K=L["K"], beta=w["beta"], row_scale=L["scale"],
+                         workspace=ws, stream=stream)
+
+
+def run_gpu(args, w, rank, world):
+    import structured_sparse_gemm_gb300 as st
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st.load()
+    layers = build_workload(w, dev, seed=rank)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        # eager warm-up (also sets kernel attributes before capture)
+        prune_phase(layers)
+        spmm_phase(layers, w)
+        stream.synchronize()
+        g_prune, g_spmm = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_prune, stream=stream):
+            prune_phase(layers)
+        with torch.cuda.graph(g_spmm, stream=stream):
+            spmm_phase(layers, w)
+    for _ in range(args.warmup):
+        g_prune.replay()
+        g_spmm.replay()
+    torch.cuda.synchronize()
+    if st.st24_device_status() != 0:
+        raise RuntimeError("device status after warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        with torch.cuda.stream(stream):
+            for k in range(args.steps):
+                ev[k][0].record(stream)
+                g_prune.replay()
+                ev[k][1].record(stream)
+                g_spmm.replay()
+                ev[k][2].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    prune_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
+    spmm_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
+    status = st.st24_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    return dict(total_ms=total_ms, prune_ms=prune_ms, spmm_ms=spmm_ms, clocks=clk.summary(),
+                layers=layers, stream=stream, g_prune=g_prune, g_spmm=g_spmm)
+
+
+def run_e2e(args, w, layers, stream):
+    """Same step through the public API with host inputs: H2D of the weights and
+    activations, prune+compress, SpMM, D2H of the outputs, all timed."""
+    import structured_sparse_gemm_gb300 as st
+
+    host = []
+    h2d = d2h = 0
+    for L in layers:
+        hA = torch.empty(L["A"].shape, dtype=L["A"].dtype, pin_memory=True)
+        hA.copy_(L["A"].cpu())
+        hX = []
+        for (X, Y, ws) in L["acts"]:
+            t = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+            t.copy_(X.cpu())
+            hX.append((t, torch.empty(Y.shape, dtype=Y.dtype, pin_memory=True)))
+            h2d += t.numel() * t.element_size()
+            d2h += Y.numel() * Y.element_size()
+        h2d += hA.numel() * hA.element_size()
+        host.append((hA, hX))
+
+    def step():
+        with torch.cuda.stream(stream):
+            for L, (hA, hX) in zip(layers, host):
+                L["A"].copy_(hA, non_blocking=True)
+                for (X, Y, ws), (hx, hy) in zip(L["acts"], hX):
+                    X.copy_(hx, non_blocking=True)
+            for L in layers:
+                st.st24_prune_compress(L["A"], L["values"], L["meta"])
+            for ni in range(len(w["Ns"])):
+                for L in layers:
+                    X, Y, ws = L["acts"][ni]
+                    st.st24_spmm(L["values"], L["meta"], X, Y, K=L["K"], beta=w["beta"], row_scale=L["scale"],
+                                 workspace=ws)
+            for L, (hA, hX) in zip(layers, host):
+                for (X, Y, ws), (hx, hy) in zip(L["acts"], hX):
+                    hy.copy_(Y, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    return ms, h2d, d2h
+
+
+def dense_context(w, dev):
+    """torch.matmul of the unpruned shapes (context only; bf16/f16 dense, int8/fp8 via bf16)."""
+    times = []
+    for (M, K) in w["shapes"]:
+        W = torch.randn(M, K, device=dev, dtype=torch.bfloat16)
+        for N in w["Ns"]:
+            X = torch.randn(N, K, device=dev, dtype=torch.bfloat16)
+            for _ in range(3):
+                X @ W.t()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(10):
+                X @ W.t()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) / 10)
+    return sum(times) * w["layers"]
+
+
+# ---------------------------------------------------------------- the oracle (CPU baseline)
+def oracle_sample(w, budget_s: float):
+    """Time the CPU oracle on a bounded sample of the workload: prune+compress of
+    the first weight, then its product with the activation widths in order,
+    repeated until about `budget_s` seconds of CPU work have been done."""
+    import oracle
+
+    M, K = w["shapes"][0]
+    g = inputs.generator(0)
+    A = inputs.raw(inputs.draw(w["ab"], (M, K), w["a_std"], g)).numpy()
+    # rows of the weight in the sample: all of them unless one SpMM pass would blow the budget
+    rows = M if M * K * max(w["Ns"]) <= 4e9 else max(128, int(4e9 // (K * max(w["Ns"]))) // 128 * 128)
+    sub = A[:rows]
+    Xs = [inputs.raw(inputs.draw(w["ab"], (N, K), 1.0, g)).numpy() for N in w["Ns"]]
+    flops, reps = 0.0, 0
+    t0 = time.perf_counter()
+    while True:
+        _, _, ov, om = oracle.prune_compress(w["ab"], sub)
+        for N, X in zip(w["Ns"], Xs):
+            oracle.spmm(w["ab"], w["c"], ov, om, X, K)
+            flops += 2.0 * rows * K * N
+        reps += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return flops, dt, oracle.default_threads(), (
+        f"{reps} x (prune+compress of {rows}x{K} weight rows and SpMM for N in {w['Ns']})")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode_bf16", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="st24", choices=["st24", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    config = {"workload": w["desc"], "name": args.workload, "shapes": w["shapes"], "Ns": w["Ns"],
+              "layers": w["layers"], "ab": w["ab"], "out": w["c"],
+              "l2": "inputs larger than L2: every step streams all weights (dense and compressed) from HBM"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        per_step, flops, threads, sample = [], 0.0, 1, ""
+        for _ in range(args.warmup):
+            oracle_sample(w, 0.0)
+        for _ in range(args.steps):
+            f, dt, threads, sample = oracle_sample(w, 8.0)
+            per_step.append(dt)
+            flops += f
+        tot = sum(per_step)
+        value = flops / tot / 1e12
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w["ab"],
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+                "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    r = run_gpu(args, w, rank, world)
+    ms_step = r["total_ms"] / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    flops = flops_per_step(w)
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    hbm, bf16_peak, bf16_sus, peak_kind = peaks()
+
+    spmm_launch_ms = r["spmm_ms"] / args.steps / n_spmm(w)
+    prune_launch_ms = r["prune_ms"] / args.steps / n_prune(w)
+    spmm_gbs = spmm_bytes(w) / (r["spmm_ms"] / args.steps * 1e-3) / 1e9
+    prune_gbs = prune_bytes(w) / (r["prune_ms"] / args.steps * 1e-3) / 1e9
+    # dominant kernel by share of the step
+    if r["spmm_ms"] >= r["prune_ms"]:
+        dom = {"kernel": "st24_spmm", "bound": "hbm", "achieved": spmm_gbs, "unit": "GB/s",
+               "bytes_per_launch": spmm_bytes(w) / n_spmm(w), "launch_us": spmm_launch_ms * 1e3}
+    else:
+        dom = {"kernel": "st24_prune_compress", "bound": "hbm", "achieved": prune_gbs, "unit": "GB/s",
+               "bytes_per_launch": prune_bytes(w) / n_prune(w), "launch_us": prune_launch_ms * 1e3}
+    roofline = {"bound": dom["bound"], "achieved": dom["achieved"], "peak": hbm, "unit": "GB/s",
+                "frac": dom["achieved"] / hbm, "traffic": None, "kernel": dom["kernel"],
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                "bytes_per_launch": dom["bytes_per_launch"], "avg_launch_us": dom["launch_us"]}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w["ab"], "data": "synthetic", "config": config,
+            "gpu_launches": args.steps * (n_spmm(w) + n_prune(w)),
+            "clocks": r["clocks"], "roofline": roofline,
+            "kernels": {"prune_compress": {"launches_per_step": n_prune(w), "us_per_launch": prune_launch_ms * 1e3,
+                                           "GB/s": prune_gbs},
+                        "spmm": {"launches_per_step": n_spmm(w), "us_per_launch": spmm_launch_ms * 1e3,
+                                 "GB/s": spmm_gbs,
+                                 "tflops_dense_equiv": flops / (r["spmm_ms"] / args.steps * 1e-3) / 1e12}}}
+    if rank == 0 and not args.no_e2e:
+        e2e_ms, h2d, d2h = run_e2e(args, w, r["layers"], r["stream"])
+        line["e2e"] = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    if rank == 0:
+        line["context"] = {"dense_torch_matmul_ms_per_step": dense_context(w, r["layers"][0]["A"].device)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f, dt, threads, sample = oracle_sample(w, 10.0)
+        line["cpu_baseline"] = {"value": f / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": sample}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

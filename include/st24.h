@@ -1,0 +1,181 @@
+/*
+ * st24.h -- C ABI of a 2:4 structured-sparse GEMM library for GB300 (sm_103a).
+ *
+ * The library implements the data-parallel hot path of 2:4 structured
+ * sparsity as described in:
+ *   [CH26] "Chapter 26 -- Sparsity: The Hardware View" (sections "2:4
+ *          Fine-Grained Structured Sparsity", "2:4 in the Memory-Bound Regime",
+ *          "Sparsity + Quantization Combine", and "Python: Build a 2:4 Mask,
+ *          Compress It, and Show Why Unstructured Doesn't Help");
+ *   [SS24] "10.4g Structured Sparsity (2:4)" (sections "What is 2:4
+ *          Structured Sparsity?" and "How Tensor Cores Leverage This Pattern").
+ *
+ * Conventions shared by every call:
+ *  - All pointers named as device buffers must point to device memory (or
+ *    memory the device can access) owned by the caller.  The library
+ *    allocates no device memory per call and keeps no pointer after a call
+ *    returns.
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  Work is enqueued asynchronously on it; a call returns once the
+ *    work is enqueued.
+ *  - Matrices use element strides (not bytes).  A is the sparse weight
+ *    (M x K, pruned along K), B the dense activation (K x N), C the output
+ *    (M x N).
+ *  - Argument errors are detected on the host before anything is enqueued
+ *    and return a status; nothing is launched in that case.  A launch failure
+ *    returns ST24_ERR_CUDA.  Errors the kernels detect while running (a wait
+ *    that ran out of time) are recorded in a per-device status word read by
+ *    st24_device_status().
+ *
+ * Compressed form (the output of st24_prune_compress, the input of
+ * st24_spmm), for an M x K matrix with K a multiple of 4:
+ *  - values: M x K/2 elements, row-major with row stride K/2; the two kept
+ *    values of group g (elements 4g..4g+3 of a row) at columns 2g and 2g+1,
+ *    in ascending order of their position in the group.  ([CH26] worked
+ *    example: values [w0 w3 | w5 w6].)
+ *  - meta: M x ceil(K/8) bytes, row-major with row stride ceil(K/8); group g
+ *    of a row is the 4-bit nibble (i0 | i1 << 2) with i0 < i1 the in-group
+ *    indices of the kept values, stored in bits 4*(g%2)..4*(g%2)+3 of byte
+ *    g/2.  ([CH26] worked example: indices [0 3 | 1 2], 2 bits each, 4 bits
+ *    per group.)  Each 32-bit little-endian word of a row therefore holds the
+ *    8 groups of 32 consecutive K, lowest K in the lowest bits, which is the
+ *    order the sparse tensor-core instructions read their metadata in.
+ */
+#ifndef ST24_H
+#define ST24_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ST24_API __attribute__((visibility("default")))
+#else
+#define ST24_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. */
+typedef enum st24_dtype {
+    ST24_F16 = 0,   /* IEEE binary16 */
+    ST24_BF16 = 1,  /* bfloat16 */
+    ST24_E4M3 = 2,  /* OCP FP8 E4M3 (finite-only "fn" variant, max 448) */
+    ST24_S8 = 3,    /* int8 */
+    ST24_F32 = 4,   /* IEEE binary32 (output only) */
+    ST24_S32 = 5    /* int32 (output only, int8 inputs) */
+} st24_dtype;
+
+typedef enum st24_status {
+    ST24_OK = 0,
+    ST24_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad stride, K % 4 != 0 */
+    ST24_ERR_UNSUPPORTED = 2,   /* valid but not handled: a type pair or a K this build rejects */
+    ST24_ERR_MISALIGNED = 3,    /* a pointer or stride breaks an alignment the call states */
+    ST24_ERR_CUDA = 4,          /* a CUDA runtime call or a launch failed */
+    ST24_ERR_TIMEOUT = 5,       /* a kernel gave up on a wait (bounded spin) and returned early */
+    ST24_ERR_WORKSPACE = 6      /* the workspace passed to st24_spmm is too small */
+} st24_status;
+
+/* Library version, (major << 16) | (minor << 8) | patch. */
+ST24_API int st24_version(void);
+
+/* A static, human-readable name for a status value. */
+ST24_API const char* st24_status_string(int status);
+
+/*
+ * Storage of the compressed form in bytes ([CH26] "The wins, quantified" and
+ * the storage accounting of its listing: half the values plus a 2-bit index
+ * per kept value).  values: M * (K/2) * sizeof(type); meta: M * ceil(K/8).
+ * For 256 x 1024 at 2 bytes per value these are 262144 and 32768 bytes
+ * (288.0 KB of a 512.0 KB dense matrix).  Return 0 for invalid arguments.
+ */
+ST24_API size_t st24_values_bytes(st24_dtype type, int64_t M, int64_t K);
+ST24_API size_t st24_meta_bytes(int64_t M, int64_t K);
+
+/*
+ * Prune and compress ([CH26] "Python: Build a 2:4 Mask, Compress It, ...":
+ * in every group of 4 consecutive elements along K keep the 2 with the
+ * largest magnitude; [SS24] "What is 2:4 Structured Sparsity?").
+ *   type   : ST24_F16, ST24_BF16, ST24_E4M3 or ST24_S8.
+ *   W      : device, M x K dense matrix, row-major, row stride ldw >= K.
+ *   values : device, st24_values_bytes(type, M, K) bytes, written.
+ *   meta   : device, st24_meta_bytes(M, K) bytes, written.
+ * Magnitude is |x|; ties go to the lower index; +0 and -0 tie; a NaN
+ * outranks every number; a group always keeps exactly two slots (a group
+ * with fewer non-zeros keeps zeros).  The result is bit-exact and
+ * deterministic.  K must be a multiple of 4; M or K == 0 is a no-op.
+ * Fast path when K*sizeof(type) % 16 == 0, W and ldw*sizeof(type) are
+ * 16-byte aligned, values 8-byte aligned and meta 2-byte aligned; any other
+ * valid layout takes a slower general kernel.
+ */
+ST24_API st24_status st24_prune_compress(st24_dtype type, const void* W, int64_t M, int64_t K, int64_t ldw,
+                                void* values, void* meta, void* stream);
+
+/*
+ * Inverse of compression ([SS24] "How Engineers Enable 2:4 Sparsity": the
+ * libraries handle compression and decompression; [CH26] pruned row
+ * [w0 0 0 w3 | 0 w5 w6 0]): writes the M x K dense matrix W (row stride
+ * ldw >= K) with the kept values at their indices and +0 elsewhere.
+ * Metadata nibbles whose two indices are not strictly ascending are not a
+ * valid compressed form; the result for such groups is unspecified (no
+ * memory outside W is written).  Same alignment fast path as above.
+ */
+ST24_API st24_status st24_decompress(st24_dtype type, const void* values, const void* meta, int64_t M,
+                            int64_t K, void* W, int64_t ldw, void* stream);
+
+/*
+ * Bytes of workspace st24_spmm needs for these sizes (0 when the chosen
+ * schedule needs none).  The workspace holds fp32 partial tiles of the
+ * split-K / stream-K schedule and one 32-bit counter per output tile.
+ * It must be zero-filled before its first use; every successful st24_spmm
+ * leaves the counters at zero again, so a workspace can be reused by later
+ * calls on the same stream without clearing.  Calls that run at the same
+ * time must not share a workspace.
+ */
+ST24_API size_t st24_spmm_workspace_bytes(st24_dtype ab_type, st24_dtype c_type, int64_t M, int64_t N,
+                                 int64_t K);
+
+/*
+ * Sparse x dense product ([CH26] "2:4 Fine-Grained Structured Sparsity": the
+ * two stored weights of each group multiply the two activations their
+ * indices select; the other two products are zero and never computed):
+ *
+ *   C(m, n) = alpha * row_scale[m] * sum_k A(m, k) * B(k, n) + beta * C(m, n)
+ *
+ *   ab_type  : ST24_F16, ST24_BF16, ST24_E4M3 (fp32 accumulation) or ST24_S8
+ *              (int32 accumulation, exact).
+ *   c_type   : ST24_F32, ST24_BF16 or ST24_F16 for any ab_type; ST24_S32
+ *              only for ST24_S8 with alpha == 1, beta == 0 and no row_scale
+ *              (the raw int32 sums).
+ *   A_values, A_meta : device, the compressed form of A (M x K).
+ *   B        : device, element (k, n) at B[n*ldb + k] (K-major; a row-major
+ *              activation X[N, K] with ldb >= K).
+ *   C        : device, element (m, n) at C[n*ldc + m] (ldc >= M; a
+ *              row-major Y[N, M]); read when beta != 0, always written.
+ *   row_scale: device, M fp32 values, or NULL for 1.
+ *   workspace: device, ws_bytes >= st24_spmm_workspace_bytes(...), or NULL
+ *              when that is 0.  See st24_spmm_workspace_bytes.
+ * The output is rounded to nearest-even from fp32 (int32 is exact).
+ * Requirements: K % 128 == 0 (ST24_ERR_UNSUPPORTED otherwise); A_values, B
+ * and A_meta 16-byte aligned; ldb*sizeof(ab_type) % 16 == 0; C aligned to
+ * its element size.  M, N == 0 is a no-op.
+ */
+ST24_API st24_status st24_spmm(st24_dtype ab_type, st24_dtype c_type, int64_t M, int64_t N, int64_t K,
+                      float alpha, const void* A_values, const void* A_meta,
+                      const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
+                      const float* row_scale, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the status word the kernels
+ * of the current device write when a bounded wait runs out
+ * (ST24_ERR_TIMEOUT), or returns ST24_ERR_CUDA if the stream reports an
+ * error.  ST24_OK otherwise.
+ */
+ST24_API st24_status st24_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ST24_H */

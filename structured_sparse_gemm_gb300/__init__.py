@@ -1,0 +1,204 @@
+"""Python binding of libst24 (2:4 structured-sparse GEMM for GB300, sm_103a).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  The functions keep the C ABI's names (include/st24.h) and take
+torch tensors for the buffers; they raise ``St24Error`` on a non-OK status.
+There is no CPU fallback: if the library is missing the import of the
+binding's functions raises.
+
+Layouts (as in the C ABI): A is the sparse weight [M, K] (pruned along K),
+B is passed as the activation X[N, K] (K-major B), C is Y[N, M].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build_lib
+
+__all__ = [
+    "St24Error", "load", "st24_version", "st24_status_string", "st24_values_bytes",
+    "st24_meta_bytes", "st24_prune_compress", "st24_decompress", "st24_spmm_workspace_bytes",
+    "st24_spmm", "st24_device_status", "dtype_code", "compress", "spmm", "Workspace",
+]
+
+F16, BF16, E4M3, S8, F32, S32 = 0, 1, 2, 3, 4, 5
+_TORCH_CODE = {
+    torch.float16: F16, torch.bfloat16: BF16, torch.float8_e4m3fn: E4M3, torch.int8: S8,
+    torch.float32: F32, torch.int32: S32,
+}
+
+
+class St24Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {st24_status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libst24.so (built in-tree by ``_build_lib.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build_lib.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"libst24 is not built ({path} missing); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    i64, p, f, sz, i = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t, ctypes.c_int
+    lib.st24_version.restype = i
+    lib.st24_status_string.argtypes = [i]
+    lib.st24_status_string.restype = ctypes.c_char_p
+    lib.st24_values_bytes.argtypes = [i, i64, i64]
+    lib.st24_values_bytes.restype = sz
+    lib.st24_meta_bytes.argtypes = [i64, i64]
+    lib.st24_meta_bytes.restype = sz
+    lib.st24_prune_compress.argtypes = [i, p, i64, i64, i64, p, p, p]
+    lib.st24_prune_compress.restype = i
+    lib.st24_decompress.argtypes = [i, p, p, i64, i64, p, i64, p]
+    lib.st24_decompress.restype = i
+    lib.st24_spmm_workspace_bytes.argtypes = [i, i, i64, i64, i64]
+    lib.st24_spmm_workspace_bytes.restype = sz
+    lib.st24_spmm.argtypes = [i, i, i64, i64, i64, f, p, p, p, i64, f, p, i64, p, p, sz, p]
+    lib.st24_spmm.restype = i
+    lib.st24_device_status.argtypes = [p]
+    lib.st24_device_status.restype = i
+    _lib = lib
+    return lib
+
+
+def dtype_code(dt) -> int:
+    if isinstance(dt, int):
+        return dt
+    if isinstance(dt, torch.dtype):
+        return _TORCH_CODE[dt]
+    return {"f16": F16, "bf16": BF16, "e4m3": E4M3, "s8": S8, "f32": F32, "s32": S32}[dt]
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise St24Error(status, what)
+
+
+def st24_version() -> int:
+    return load().st24_version()
+
+
+def st24_status_string(status: int) -> str:
+    return load().st24_status_string(status).decode()
+
+
+def st24_values_bytes(dt, M: int, K: int) -> int:
+    return load().st24_values_bytes(dtype_code(dt), M, K)
+
+
+def st24_meta_bytes(M: int, K: int) -> int:
+    return load().st24_meta_bytes(M, K)
+
+
+def st24_prune_compress(W: torch.Tensor, values: torch.Tensor, meta: torch.Tensor, *, stream=None) -> None:
+    """Prune W [M, K] (row stride W.stride(0)) to 2:4 and write its compressed form."""
+    M, K = W.shape
+    if W.stride(1) != 1:
+        raise ValueError("W must have unit stride along K")
+    _check(load().st24_prune_compress(dtype_code(W.dtype), _ptr(W), M, K, W.stride(0), _ptr(values),
+                                      _ptr(meta), _stream(stream)), "st24_prune_compress")
+
+
+def st24_decompress(values: torch.Tensor, meta: torch.Tensor, W: torch.Tensor, *, stream=None) -> None:
+    """Expand a compressed form into W [M, K] (+0 at dropped positions)."""
+    M, K = W.shape
+    if W.stride(1) != 1:
+        raise ValueError("W must have unit stride along K")
+    _check(load().st24_decompress(dtype_code(W.dtype), _ptr(values), _ptr(meta), M, K, _ptr(W),
+                                  W.stride(0), _stream(stream)), "st24_decompress")
+
+
+def st24_spmm_workspace_bytes(ab, c, M: int, N: int, K: int) -> int:
+    return load().st24_spmm_workspace_bytes(dtype_code(ab), dtype_code(c), M, N, K)
+
+
+def st24_spmm(values: torch.Tensor, meta: torch.Tensor, X: torch.Tensor, Y: torch.Tensor, *, K: int | None = None,
+              alpha: float = 1.0, beta: float = 0.0, row_scale: torch.Tensor | None = None,
+              workspace: torch.Tensor | None = None, M: int | None = None, stream=None) -> None:
+    """Y[N, M] = alpha * row_scale * (A_sparse @ X.T).T + beta * Y, A given by (values, meta)."""
+    N, Kx = X.shape
+    K = Kx if K is None else K
+    M = Y.shape[1] if M is None else M
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if X.stride(1) != 1 or Y.stride(1) != 1:
+        raise ValueError("X and Y must have unit stride along their last dimension")
+    _check(load().st24_spmm(dtype_code(X.dtype), dtype_code(Y.dtype), M, N, K, float(alpha), _ptr(values),
+                            _ptr(meta), _ptr(X), X.stride(0), float(beta), _ptr(Y), Y.stride(0),
+                            _ptr(row_scale), _ptr(workspace), ws_bytes, _stream(stream)), "st24_spmm")
+
+
+def st24_device_status(stream=None) -> int:
+    return load().st24_device_status(_stream(stream))
+
+
+# ---- conveniences (allocation through torch; compute still in the library) ----
+
+def compress(W: torch.Tensor, *, stream=None):
+    """(values, meta) of W [M, K] on W's device."""
+    M, K = W.shape
+    values = torch.empty((M, K // 2), dtype=W.dtype, device=W.device)
+    meta = torch.empty((M, (K // 4 + 1) // 2), dtype=torch.uint8, device=W.device)
+    st24_prune_compress(W, values, meta, stream=stream)
+    return values, meta
+
+
+class Workspace:
+    """A zero-filled workspace per (device, size), reused across calls on one stream."""
+
+    def __init__(self):
+        self._bufs = {}
+
+    def get(self, nbytes: int, device) -> torch.Tensor | None:
+        if nbytes == 0:
+            return None
+        key = (str(device),)
+        buf = self._bufs.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+            self._bufs[key] = buf
+        return buf
+
+
+_default_ws = Workspace()
+
+
+def spmm(values: torch.Tensor, meta: torch.Tensor, X: torch.Tensor, *, out_dtype=torch.bfloat16,
+         alpha: float = 1.0, beta: float = 0.0, C: torch.Tensor | None = None,
+         row_scale: torch.Tensor | None = None, workspace: Workspace | None = None, stream=None):
+    """Y[N, M] = alpha * row_scale * (A_sparse @ X.T).T + beta * C."""
+    M = values.shape[0]
+    N, K = X.shape
+    if C is not None:
+        Y = C
+    else:
+        Y = torch.empty((N, M), dtype=out_dtype, device=X.device)
+    ws = (workspace or _default_ws).get(st24_spmm_workspace_bytes(X.dtype, Y.dtype, M, N, K), X.device)
+    st24_spmm(values, meta, X, Y, K=K, alpha=alpha, beta=beta, row_scale=row_scale, workspace=ws,
+              M=M, stream=stream)
+    return Y

@@ -1,0 +1,447 @@
+// spmm_mmasp.cuh -- C = alpha * row_scale * (A_sparse * B) + beta * C on the
+// warp-level sparse tensor-core instruction (mma.sp::ordered_metadata).
+//
+// Method ("Chapter 26 -- Sparsity: The Hardware View", section "2:4
+// Fine-Grained Structured Sparsity"): the metadata of each group selects the
+// two activations its two stored weights multiply; the other two products are
+// zero and never computed.  A is streamed in its compressed form (values +
+// metadata), so for small N the kernel reads ~56% of the dense weight bytes
+// (section "2:4 in the Memory-Bound Regime").
+//
+// Structure (one CTA per SM, persistent):
+//  * Schedule: stream-K.  The (output tile, k-block) iterations are flattened
+//    and each CTA takes one contiguous run of them, so every SM streams the
+//    same number of A bytes whatever the tile count.  A tile whose k-blocks
+//    are spread over several CTAs is finished by whichever of them arrives
+//    last: each writes its fp32 (or int32) partial tile to the workspace and
+//    bumps the tile's counter; the last one sums the partials in k order
+//    (deterministic), applies the epilogue and resets the counter.
+//  * Producer warp: TMA loads of the compressed A tile (128-byte swizzle), the
+//    A metadata tile and the B tile (128-byte swizzle) into a ring of stages
+//    guarded by full/empty mbarriers.
+//  * Consumer warps (4 x WARPS_N): ldmatrix fragments, mma.sp into registers.
+//  * Epilogue: alpha, per-row scale, beta * C, rounding to the output type.
+#pragma once
+#include "st24_device.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+namespace st24 {
+namespace mmasp {
+
+// Per element type: 16-bit types use m16n8k32 (32 logical K per MMA, 128 per
+// k-block); 8-bit types use m16n8k64 (64 per MMA, 256 per k-block).  Either
+// way one k-block is 128 bytes of compressed A per row, 256 bytes of B per
+// column, and EB bytes of metadata per row.
+template <int DT>
+struct Traits {
+  static constexpr int ES = (DT == kF16 || DT == kBF16) ? 2 : 1;
+  static constexpr int KSTEP = 64 / ES;      // logical K of one MMA
+  static constexpr int BK = 4 * KSTEP;       // logical K of one k-block
+  static constexpr int EB = BK / 8;          // metadata bytes per row per k-block
+  static constexpr bool kInt = DT == kS8;
+};
+
+template <int DT, int BN_, int WARPS_N_, int STAGES_>
+struct Config {
+  using T = Traits<DT>;
+  static constexpr int BM = 128;
+  static constexpr int BN = BN_;
+  static constexpr int WARPS_M = 4;
+  static constexpr int WARPS_N = WARPS_N_;
+  static constexpr int CONSUMERS = WARPS_M * WARPS_N;
+  static constexpr int THREADS = (CONSUMERS + 1) * 32;
+  static constexpr int WN = BN / 8 / WARPS_N;        // n8 tiles per warp
+  static constexpr int STAGES = STAGES_;
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 256;           // two 128-byte-wide boxes
+  static constexpr int E_BYTES = BM * T::EB;
+  static constexpr int STAGE_TX = A_BYTES + B_BYTES + E_BYTES;
+  static constexpr int STAGE_BYTES = (STAGE_TX + 1023) / 1024 * 1024;
+  static constexpr int PARTIAL_ELEMS = BM * BN;      // one fp32/int32 partial tile
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static_assert(WN >= 1 && BN % (8 * WARPS_N) == 0, "tile split");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+struct Params {
+  int64_t M, N, K;
+  int64_t tiles_n, k_iters, total_iters;
+  float alpha, beta;
+  void* C;
+  int64_t ldc;
+  int c_type;
+  const float* row_scale;
+  float* partials;       // [2 * gridDim.x][PARTIAL_ELEMS]
+  unsigned* counters;    // one per output tile
+  unsigned* status;
+};
+
+// ---- schedule helpers ---------------------------------------------------------
+__device__ __forceinline__ int64_t iter_begin(int64_t c, int64_t T, int64_t G) { return c * T / G; }
+// The CTA whose run contains iteration u.
+__device__ __forceinline__ int64_t iter_owner(int64_t u, int64_t T, int64_t G) {
+  return ((u + 1) * G - 1) / T;
+}
+
+// ---- output -------------------------------------------------------------------
+__device__ __forceinline__ float load_c(const Params& p, int64_t idx) {
+  switch (p.c_type) {
+    case kF32: return static_cast<const float*>(p.C)[idx];
+    case kBF16: return __bfloat162float(static_cast<const __nv_bfloat16*>(p.C)[idx]);
+    default: return __half2float(static_cast<const __half*>(p.C)[idx]);
+  }
+}
+
+template <typename Acc>
+__device__ __forceinline__ void store_out(const Params& p, int64_t m, int64_t n, Acc acc) {
+  const int64_t idx = n * p.ldc + m;
+  if constexpr (std::is_same<Acc, int>::value) {
+    if (p.c_type == kS32) {
+      static_cast<int*>(p.C)[idx] = acc;
+      return;
+    }
+  }
+  const float a = static_cast<float>(acc);
+  const float s = p.row_scale ? __fmul_rn(p.alpha, p.row_scale[m]) : p.alpha;
+  float r = __fmul_rn(a, s);
+  if (p.beta != 0.0f) r = __fadd_rn(r, __fmul_rn(p.beta, load_c(p, idx)));
+  switch (p.c_type) {
+    case kF32: static_cast<float*>(p.C)[idx] = r; break;
+    case kBF16: static_cast<__nv_bfloat16*>(p.C)[idx] = __float2bfloat16_rn(r); break;
+    default: static_cast<__half*>(p.C)[idx] = __float2half_rn(r); break;
+  }
+}
+
+__device__ __forceinline__ void consumer_sync(int threads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
+}
+
+// Metadata register of lane `lane` for each k-step of an m16 tile whose rows
+// start at `row0` in the stage's metadata block (EB bytes per row, canonical
+// order: 8 groups per 32-bit word, lowest K in the lowest nibble).
+// Lane layout of the metadata operand (sparsity selector 0), with g = lane/4:
+//  m16n8k32, 16-bit types: lane 4g supplies groups 0-3 of the k-step, row g in
+//    its low 16 bits and row g+8 in its high 16 bits; lane 4g+1 the same for
+//    groups 4-7.  (Lanes 4g+2, 4g+3 are not read.)
+//  m16n8k64, 8-bit types: lane 4g+t supplies 8 groups of row g + 8*(t&1),
+//    groups 0-7 of the k-step for t < 2 and groups 8-15 for t >= 2.
+// Rows past M were zero-filled by the TMA; they get a valid index pair (0, 1).
+template <int DT>
+__device__ __forceinline__ void meta_words(const uint8_t* sE, int row0, int lane, int64_t rows_left,
+                                           uint32_t (&w)[4]) {
+  using T = Traits<DT>;
+  const int g = lane >> 2, t = lane & 3;
+  if constexpr (T::ES == 2) {
+    uint4 lo = *reinterpret_cast<const uint4*>(sE + (row0 + g) * T::EB);
+    uint4 hi = *reinterpret_cast<const uint4*>(sE + (row0 + g + 8) * T::EB);
+    if (g >= rows_left) lo = make_uint4(0x44444444u, 0x44444444u, 0x44444444u, 0x44444444u);
+    if (g + 8 >= rows_left) hi = make_uint4(0x44444444u, 0x44444444u, 0x44444444u, 0x44444444u);
+    const uint32_t sel = (t & 1) ? 0x7632u : 0x5410u;
+    w[0] = __byte_perm(lo.x, hi.x, sel);
+    w[1] = __byte_perm(lo.y, hi.y, sel);
+    w[2] = __byte_perm(lo.z, hi.z, sel);
+    w[3] = __byte_perm(lo.w, hi.w, sel);
+  } else {
+    const int r = g + 8 * (t & 1);
+    const int half = t >> 1;
+    const uint8_t* rowp = sE + (row0 + r) * T::EB;
+    const uint4 lo = *reinterpret_cast<const uint4*>(rowp);
+    const uint4 hi = *reinterpret_cast<const uint4*>(rowp + 16);
+    w[0] = half ? lo.y : lo.x;
+    w[1] = half ? lo.w : lo.z;
+    w[2] = half ? hi.y : hi.x;
+    w[3] = half ? hi.w : hi.z;
+    if (r >= rows_left) w[0] = w[1] = w[2] = w[3] = 0x44444444u;
+  }
+}
+
+template <int DT, int BN, int WARPS_N, int STAGES>
+__global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
+    spmm_mmasp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmE,
+                      const __grid_constant__ CUtensorMap tmB, const Params p) {
+  using Cfg = Config<DT, BN, WARPS_N, STAGES>;
+  using T = Traits<DT>;
+  using Acc = typename std::conditional<T::kInt, int, float>::type;
+  constexpr int WN = Cfg::WN;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + STAGES;
+  int* s_last = reinterpret_cast<int*>(empty_bar + STAGES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t G = gridDim.x, cta = blockIdx.x;
+  const int64_t Ttot = p.total_iters, KI = p.k_iters;
+  const int64_t it_begin = iter_begin(cta, Ttot, G), it_end = iter_begin(cta + 1, Ttot, G);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), Cfg::CONSUMERS);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == Cfg::CONSUMERS) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmE);
+      tma_prefetch_desc(&tmB);
+      const uint64_t stream_once = policy_evict_first();
+      const uint64_t reuse = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_parity[STAGES];
+      bool issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = false;
+      bool ok = true;
+      for (int64_t it = it_begin; it < it_end && ok;) {
+        const int64_t tile = it / KI;
+        const int64_t kb0 = it - tile * KI;
+        const int64_t kb1 = min(KI, kb0 + (it_end - it));
+        const int32_t mt = static_cast<int32_t>(tile / p.tiles_n);
+        const int32_t nt = static_cast<int32_t>(tile - static_cast<int64_t>(mt) * p.tiles_n);
+        for (int64_t kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&full_bar[stage]);
+          mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
+          uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
+          const int32_t ka = static_cast<int32_t>(kb * (128 / T::ES));   // compressed A column
+          const int32_t kB = static_cast<int32_t>(kb * T::BK);           // logical K
+          tma_load_2d(smem_u32(st), &tmA, ka, mt * Cfg::BM, fb, stream_once);
+          tma_load_2d(smem_u32(st + Cfg::A_BYTES), &tmB, kB, nt * BN, fb, reuse);
+          tma_load_2d(smem_u32(st + Cfg::A_BYTES + BN * 128), &tmB, kB + 128 / T::ES, nt * BN, fb, reuse);
+          tma_load_2d(smem_u32(st + Cfg::A_BYTES + Cfg::B_BYTES), &tmE,
+                      static_cast<int32_t>(kb * T::EB), mt * Cfg::BM, fb, stream_once);
+          issued[stage] = true;
+          issued_parity[stage] = phase;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        it += kb1 - kb0;
+      }
+      // Never leave with copies in flight into this CTA's shared memory.
+      for (int s = 0; s < STAGES; ++s)
+        if (issued[s]) mbar_wait(smem_u32(&full_bar[s]), issued_parity[s], p.status);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int wm = warp % Cfg::WARPS_M, wn = warp / Cfg::WARPS_M;
+  const int gid = lane >> 2, tig = lane & 3;
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int64_t it = it_begin; it < it_end;) {
+    const int64_t tile = it / KI;
+    const int64_t kb0 = it - tile * KI;
+    const int64_t kb1 = min(KI, kb0 + (it_end - it));
+    const int64_t mt = tile / p.tiles_n, nt = tile - mt * p.tiles_n;
+    const int64_t m_base = mt * Cfg::BM, n_base = nt * BN;
+    Acc acc[2][WN][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int j = 0; j < WN; ++j)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[i][j][r] = 0;
+
+    bool ok = true;
+    for (int64_t kb = kb0; kb < kb1; ++kb) {
+      if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.status)) { ok = false; break; }
+      const uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
+      const uint32_t sA = smem_u32(st);
+      const uint32_t sB = smem_u32(st + Cfg::A_BYTES);
+      const uint8_t* sE = st + Cfg::A_BYTES + Cfg::B_BYTES;
+      uint32_t e[2][4];
+      meta_words<DT>(sE, wm * 32, lane, p.M - m_base - wm * 32, e[0]);
+      meta_words<DT>(sE, wm * 32 + 16, lane, p.M - m_base - wm * 32 - 16, e[1]);
+      const int64_t ks_left = (p.K - kb * T::BK) / T::KSTEP;
+      const int ksteps = ks_left < 4 ? static_cast<int>(ks_left) : 4;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        if (ks >= ksteps) break;
+        uint32_t a[2][4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int q = lane >> 3, r8 = lane & 7;
+          const int row = wm * 32 + i * 16 + (q & 1) * 8 + r8;
+          const int chunk = ks * 2 + (q >> 1);
+          ldmatrix_x4(sA + row * 128 + ((chunk ^ (row & 7)) << 4), a[i][0], a[i][1], a[i][2], a[i][3]);
+        }
+#pragma unroll
+        for (int j = 0; j < WN; ++j) {
+          const int q = lane >> 3, r8 = lane & 7;
+          const int n = wn * WN * 8 + j * 8 + r8;
+          const int box = ks >> 1, cb = (ks & 1) * 4 + q;
+          uint32_t b[4];
+          ldmatrix_x4(sB + box * (BN * 128) + n * 128 + ((cb ^ (n & 7)) << 4), b[0], b[1], b[2], b[3]);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            if constexpr (DT == kS8)
+              mma_sp_16864_s8(acc[i][j], a[i], b, e[i][ks]);
+            else if constexpr (DT == kE4M3)
+              mma_sp_16864_e4m3(acc[i][j], a[i], b, e[i][ks]);
+            else
+              mma_sp_16832<DT>(acc[i][j], a[i], b, e[i][ks]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty_bar[stage]));
+      if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+    }
+    if (!ok) break;
+
+    // ---- epilogue ----
+    const bool whole = (kb0 == 0 && kb1 == KI);
+    bool write_out = whole;
+    if (!whole) {
+      // Partial tile: publish it, and let the last contributor finish the tile.
+      const int64_t c_lo = iter_owner(tile * KI, Ttot, G);
+      const int64_t c_hi = iter_owner(tile * KI + KI - 1, Ttot, G);
+      auto slot_of = [&](int64_t c) -> int64_t {
+        return 2 * c + ((iter_begin(c, Ttot, G) / KI) == tile ? 0 : 1);
+      };
+      float4* mine = reinterpret_cast<float4*>(p.partials + slot_of(cta) * Cfg::PARTIAL_ELEMS);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < WN; ++j) {
+          const int idx = ((warp * 2 + i) * WN + j) * 32 + lane;
+          float4 v;
+          if constexpr (T::kInt) {
+            v = make_float4(__int_as_float(acc[i][j][0]), __int_as_float(acc[i][j][1]),
+                            __int_as_float(acc[i][j][2]), __int_as_float(acc[i][j][3]));
+          } else {
+            v = make_float4(acc[i][j][0], acc[i][j][1], acc[i][j][2], acc[i][j][3]);
+          }
+          __stcg(mine + idx, v);
+        }
+      __threadfence();
+      consumer_sync(Cfg::CONSUMERS * 32);
+      if (threadIdx.x == 0) {
+        const unsigned nseg = static_cast<unsigned>(c_hi - c_lo + 1);
+        const unsigned old = atomicAdd(p.counters + tile, 1u);
+        const int last = (old == nseg - 1) ? 1 : 0;
+        if (last) p.counters[tile] = 0;   // every contributor has arrived: reset for the next call
+        __threadfence();
+        *s_last = last;
+      }
+      consumer_sync(Cfg::CONSUMERS * 32);
+      write_out = *s_last != 0;
+      if (write_out) {
+        // Sum the partials in k order (segment c_lo first), one fragment at a
+        // time; this CTA's own partial is taken from its registers.
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int j = 0; j < WN; ++j) {
+            const int idx = ((warp * 2 + i) * WN + j) * 32 + lane;
+            Acc t[4];
+            for (int64_t c = c_lo; c <= c_hi; ++c) {
+              Acc v[4];
+              if (c == cta) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) v[r] = acc[i][j][r];
+              } else {
+                const float4 f =
+                    __ldcg(reinterpret_cast<const float4*>(p.partials + slot_of(c) * Cfg::PARTIAL_ELEMS) + idx);
+                if constexpr (T::kInt) {
+                  v[0] = __float_as_int(f.x); v[1] = __float_as_int(f.y);
+                  v[2] = __float_as_int(f.z); v[3] = __float_as_int(f.w);
+                } else {
+                  v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+                }
+              }
+#pragma unroll
+              for (int r = 0; r < 4; ++r) t[r] = (c == c_lo) ? v[r] : t[r] + v[r];
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[i][j][r] = t[r];
+          }
+      }
+    }
+    if (write_out) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < WN; ++j)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int64_t m = m_base + wm * 32 + i * 16 + gid + 8 * (r >> 1);
+            const int64_t n = n_base + wn * WN * 8 + j * 8 + 2 * tig + (r & 1);
+            if (m < p.M && n < p.N) store_out<Acc>(p, m, n, acc[i][j][r]);
+          }
+    }
+    it += kb1 - kb0;
+  }
+}
+
+template <int DT, int BN, int WARPS_N, int STAGES>
+st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev,
+                       cudaStream_t stream) {
+  using Cfg = Config<DT, BN, WARPS_N, STAGES>;
+  using T = Traits<DT>;
+  const CUtensorMapDataType ty = T::ES == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUtensorMap tmA, tmE, tmB;
+  const uint64_t kc = a.K / 2;  // compressed columns
+  if (!encode_tensor_map_2d(&tmA, ty, a.values, kc, a.M, kc * T::ES, 128 / T::ES, Cfg::BM,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tensor_map_2d(&tmE, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.meta, a.K / 8, a.M, a.K / 8,
+                            T::EB, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_tensor_map_2d(&tmB, ty, a.B, a.K, a.N, a.ldb * T::ES, 128 / T::ES, BN,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+    return ST24_ERR_CUDA;
+  Params p{};
+  p.M = a.M; p.N = a.N; p.K = a.K;
+  p.tiles_n = plan.tiles_n;
+  p.k_iters = plan.k_iters;
+  p.total_iters = plan.total_iters;
+  p.alpha = a.alpha; p.beta = a.beta;
+  p.C = a.C; p.ldc = a.ldc; p.c_type = a.c;
+  p.row_scale = a.row_scale;
+  p.partials = static_cast<float*>(a.workspace);
+  p.counters = plan.ws_bytes
+                   ? reinterpret_cast<unsigned*>(static_cast<uint8_t*>(a.workspace) +
+                                                 2 * static_cast<size_t>(plan.grid) * plan.partial_bytes)
+                   : nullptr;
+  p.status = dev.status;
+  auto kern = spmm_mmasp_kernel<DT, BN, WARPS_N, STAGES>;
+  static bool attr_set[64] = {};
+  if (!attr_set[dev.device % 64]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
+        cudaSuccess)
+      return ST24_ERR_CUDA;
+    attr_set[dev.device % 64] = true;
+  }
+  kern<<<plan.grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmE, tmB, p);
+  return cudaGetLastError() == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;
+}
+
+template <int DT>
+st24_status launch_dt_impl(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev,
+                      cudaStream_t s) {
+  constexpr bool k16 = Traits<DT>::ES == 2;
+  switch (plan.bn) {
+    case 8: return launch_cfg<DT, 8, 1, 8>(a, plan, dev, s);
+    case 16: return launch_cfg<DT, 16, 1, 8>(a, plan, dev, s);
+    case 32: return launch_cfg<DT, 32, 1, k16 ? 7 : 6>(a, plan, dev, s);
+    case 64: return launch_cfg<DT, 64, 1, k16 ? 6 : 5>(a, plan, dev, s);
+    default: return launch_cfg<DT, 128, 2, 4>(a, plan, dev, s);
+  }
+}
+
+// Entry per element type (defined, one per translation unit, in spmm_mmasp_<type>.cu).
+template <int DT>
+st24_status launch_dt(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev,
+                      cudaStream_t s);
+
+}  // namespace mmasp
+}  // namespace st24

@@ -1,0 +1,199 @@
+// st24_api.cu -- the C ABI (include/st24.h): argument checks, per-device state,
+// schedule choice and kernel launch.  Every argument error is caught here, on
+// the host, before any CUDA call is made.
+#include <mutex>
+
+#include "st24_device.cuh"
+
+namespace st24 {
+
+namespace {
+
+// The status word kernels write when a bounded wait runs out.  One per device
+// that loads the library; its address is looked up per device.
+__device__ unsigned g_status_word;
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_info[kMaxDevices];
+std::once_flag g_once[kMaxDevices];
+
+bool is_ab_type(int t) { return t == kF16 || t == kBF16 || t == kE4M3 || t == kS8; }
+
+bool aligned(const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+}  // namespace
+
+const DeviceInfo* current_device_info() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::call_once(g_once[dev], [dev] {
+    DeviceInfo info;
+    int sms = 0;
+    void* word = nullptr;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return;
+    if (cudaGetSymbolAddress(&word, g_status_word) != cudaSuccess) return;
+    info.device = dev;
+    info.num_sms = sms;
+    info.status = static_cast<unsigned*>(word);
+    g_info[dev] = info;
+  });
+  return g_info[dev].device == dev ? &g_info[dev] : nullptr;
+}
+
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base,
+                          uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                          uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace st24
+
+using namespace st24;
+
+extern "C" {
+
+int st24_version(void) { return (0 << 16) | (1 << 8) | 0; }
+
+const char* st24_status_string(int status) {
+  switch (status) {
+    case ST24_OK: return "ok";
+    case ST24_ERR_INVALID_ARG: return "invalid argument";
+    case ST24_ERR_UNSUPPORTED: return "unsupported (type pair or shape)";
+    case ST24_ERR_MISALIGNED: return "misaligned pointer or stride";
+    case ST24_ERR_CUDA: return "CUDA error";
+    case ST24_ERR_TIMEOUT: return "a kernel wait timed out";
+    case ST24_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+size_t st24_values_bytes(st24_dtype type, int64_t M, int64_t K) {
+  if (!is_ab_type(type) || M < 0 || K < 0 || K % 4 != 0) return 0;
+  return static_cast<size_t>(M) * static_cast<size_t>(K / 2) * elem_size(type);
+}
+
+size_t st24_meta_bytes(int64_t M, int64_t K) {
+  if (M < 0 || K < 0 || K % 4 != 0) return 0;
+  return static_cast<size_t>(M) * static_cast<size_t>(meta_row_bytes(K));
+}
+
+st24_status st24_prune_compress(st24_dtype type, const void* W, int64_t M, int64_t K, int64_t ldw,
+                                void* values, void* meta, void* stream) {
+  if (!is_ab_type(type) || M < 0 || K < 0 || K % 4 != 0) return ST24_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return ST24_OK;
+  if (!W || !values || !meta || ldw < K) return ST24_ERR_INVALID_ARG;
+  return launch_prune_compress(type, W, M, K, ldw, values, meta, static_cast<cudaStream_t>(stream));
+}
+
+st24_status st24_decompress(st24_dtype type, const void* values, const void* meta, int64_t M,
+                            int64_t K, void* W, int64_t ldw, void* stream) {
+  if (!is_ab_type(type) || M < 0 || K < 0 || K % 4 != 0) return ST24_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return ST24_OK;
+  if (!W || !values || !meta || ldw < K) return ST24_ERR_INVALID_ARG;
+  return launch_decompress(type, values, meta, M, K, W, ldw, static_cast<cudaStream_t>(stream));
+}
+
+static st24_status check_spmm(const SpmmArgs& a) {
+  if (!is_ab_type(a.ab) || a.M < 0 || a.N < 0 || a.K < 0 || a.K % 4 != 0)
+    return ST24_ERR_INVALID_ARG;
+  const bool float_out = a.c == kF32 || a.c == kBF16 || a.c == kF16;
+  if (!float_out && !(a.c == kS32 && a.ab == kS8)) return ST24_ERR_UNSUPPORTED;
+  if (a.c == kS32 && (a.alpha != 1.0f || a.beta != 0.0f || a.row_scale))
+    return ST24_ERR_UNSUPPORTED;
+  if (a.M == 0 || a.N == 0) return ST24_OK;
+  if (!a.C || a.ldc < a.M) return ST24_ERR_INVALID_ARG;
+  if (a.K > 0 && (!a.values || !a.meta || !a.B || a.ldb < a.K)) return ST24_ERR_INVALID_ARG;
+  if (a.K % 128 != 0) return ST24_ERR_UNSUPPORTED;
+  const int es = elem_size(a.ab);
+  if (a.K > 0 && (!aligned(a.values, 16) || !aligned(a.meta, 16) || !aligned(a.B, 16) ||
+                  (a.ldb * es) % 16 != 0))
+    return ST24_ERR_MISALIGNED;
+  if (!aligned(a.C, elem_size(a.c)) || (a.row_scale && !aligned(a.row_scale, 4)))
+    return ST24_ERR_MISALIGNED;
+  return ST24_OK;
+}
+
+size_t st24_spmm_workspace_bytes(st24_dtype ab_type, st24_dtype c_type, int64_t M, int64_t N,
+                                 int64_t K) {
+  if (!is_ab_type(ab_type) || M <= 0 || N <= 0 || K <= 0 || K % 128 != 0) return 0;
+  const DeviceInfo* dev = current_device_info();
+  if (!dev) return 0;
+  SpmmArgs a{};
+  a.ab = ab_type;
+  a.c = c_type;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  return plan_spmm_mmasp(a, dev->num_sms).ws_bytes;
+}
+
+st24_status st24_spmm(st24_dtype ab_type, st24_dtype c_type, int64_t M, int64_t N, int64_t K,
+                      float alpha, const void* A_values, const void* A_meta, const void* B,
+                      int64_t ldb, float beta, void* C, int64_t ldc, const float* row_scale,
+                      void* workspace, size_t ws_bytes, void* stream) {
+  SpmmArgs a{};
+  a.ab = ab_type;
+  a.c = c_type;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.alpha = alpha;
+  a.beta = beta;
+  a.values = A_values;
+  a.meta = A_meta;
+  a.B = B;
+  a.ldb = ldb;
+  a.C = C;
+  a.ldc = ldc;
+  a.row_scale = row_scale;
+  a.workspace = workspace;
+  a.ws_bytes = ws_bytes;
+  st24_status st = check_spmm(a);
+  if (st != ST24_OK || M == 0 || N == 0) return st;
+  const DeviceInfo* dev = current_device_info();
+  if (!dev) return ST24_ERR_CUDA;
+  const StreamKPlan plan = plan_spmm_mmasp(a, dev->num_sms);
+  if (plan.ws_bytes > 0 && (!workspace || ws_bytes < plan.ws_bytes || !aligned(workspace, 16)))
+    return ST24_ERR_WORKSPACE;
+  return launch_spmm_mmasp(a, plan, *dev, static_cast<cudaStream_t>(stream));
+}
+
+st24_status st24_device_status(void* stream) {
+  const DeviceInfo* dev = current_device_info();
+  if (!dev) return ST24_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ST24_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, dev->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ST24_ERR_CUDA;
+  if (word == 0) return ST24_OK;
+  if (cudaMemset(dev->status, 0, sizeof word) != cudaSuccess) return ST24_ERR_CUDA;
+  return (word & kStatusTimeout) ? ST24_ERR_TIMEOUT : ST24_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,86 @@
+// st24_internal.h -- declarations shared between the C-ABI layer (st24_api.cu)
+// and the kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/st24.h"
+
+namespace st24 {
+
+constexpr int kF16 = ST24_F16;
+constexpr int kBF16 = ST24_BF16;
+constexpr int kE4M3 = ST24_E4M3;
+constexpr int kS8 = ST24_S8;
+constexpr int kF32 = ST24_F32;
+constexpr int kS32 = ST24_S32;
+
+__host__ __device__ inline int elem_size(int dt) {
+  switch (dt) {
+    case kF16: case kBF16: return 2;
+    case kE4M3: case kS8: return 1;
+    case kF32: case kS32: return 4;
+    default: return 0;
+  }
+}
+
+__host__ __device__ inline int64_t meta_row_bytes(int64_t K) { return (K / 4 + 1) / 2; }
+
+// Per-device state the launchers need.
+struct DeviceInfo {
+  int device = -1;
+  int num_sms = 0;
+  unsigned* status = nullptr;   // device address of this device's status word
+};
+// Info for the current device (queried once per device).  nullptr on failure.
+const DeviceInfo* current_device_info();
+
+// ---------------------------------------------------------- prune / compress
+st24_status launch_prune_compress(int dt, const void* W, int64_t M, int64_t K, int64_t ldw,
+                                  void* values, void* meta, cudaStream_t stream);
+st24_status launch_decompress(int dt, const void* values, const void* meta, int64_t M, int64_t K,
+                              void* W, int64_t ldw, cudaStream_t stream);
+
+// ---------------------------------------------------------------- SpMM
+struct SpmmArgs {
+  int ab, c;
+  int64_t M, N, K;
+  float alpha, beta;
+  const void* values;
+  const void* meta;
+  const void* B;
+  int64_t ldb;
+  void* C;
+  int64_t ldc;
+  const float* row_scale;
+  void* workspace;
+  size_t ws_bytes;
+};
+
+// A split of the output into tiles and of each tile's K loop into iterations,
+// shared out over a persistent grid (stream-K: every CTA gets a contiguous
+// run of the flattened (tile, k-iteration) space).
+struct StreamKPlan {
+  int bm, bn, bk;          // tile shape; bk in logical K
+  int64_t tiles_m, tiles_n, k_iters;
+  int64_t total_iters;
+  int grid;                // CTAs
+  size_t partial_bytes;    // bytes of one fp32 partial tile
+  size_t ws_bytes;         // workspace bytes (0 if no tile is split)
+};
+
+// The mma.sp (warp-level sparse MMA) path: every element type.
+StreamKPlan plan_spmm_mmasp(const SpmmArgs& a, int num_sms);
+st24_status launch_spmm_mmasp(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev,
+                              cudaStream_t stream);
+
+// Tensor maps (driver entry point fetched through the runtime, so the library
+// has no link-time dependency on libcuda).
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base,
+                          uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                          uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+}  // namespace st24

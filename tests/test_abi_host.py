@@ -1,0 +1,98 @@
+"""The C-ABI library loads, exports every symbol its header declares, and
+rejects bad arguments on the host (no GPU needed for any of this)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import oracle
+import structured_sparse_gemm_gb300 as st
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(st24_\w+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from structured_sparse_gemm_gb300 import _build_lib
+    _build_lib.build()
+    return st.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"st24_prune_compress", "st24_decompress", "st24_spmm"} <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", st._build_lib.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (st24_\w+)$", out, flags=re.M))
+    for n in names:
+        assert n in exported, n
+        getattr(lib, n)
+    # nothing else leaks out under the st24_ prefix
+    assert exported == set(names)
+
+
+def test_sizes_match_oracle_closed_form(lib):
+    # 256 x 1024 at 2 bytes per value: 256 KiB of values + 32 KiB of metadata = 288.0 KB.
+    assert st.st24_values_bytes("f16", 256, 1024) == oracle.values_bytes("f16", 256, 1024) == 262144
+    assert st.st24_meta_bytes(256, 1024) == oracle.meta_bytes(256, 1024) == 32768
+    for dt in ("f16", "bf16", "e4m3", "s8"):
+        for M, K in ((1, 4), (3, 12), (7, 1000), (28672, 8192)):
+            assert st.st24_values_bytes(dt, M, K) == oracle.values_bytes(dt, M, K)
+            assert st.st24_meta_bytes(M, K) == oracle.meta_bytes(M, K)
+    assert st.st24_values_bytes("f16", 4, 6) == 0       # K % 4 != 0
+    assert st.st24_values_bytes("f32", 4, 8) == 0       # not an input type
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert st.st24_status_string(s) and st.st24_status_string(s) != "unknown status"
+    assert st.st24_status_string(99) == "unknown status"
+    assert st.st24_version() > 0
+
+
+FAKE = 1 << 20   # an aligned non-null address; never dereferenced: the checks run first
+
+
+def test_prune_compress_rejects_bad_arguments(lib):
+    f = lib.st24_prune_compress
+    assert f(st.BF16, FAKE, 4, 6, 6, FAKE, FAKE, None) == 1        # K % 4
+    assert f(st.F32, FAKE, 4, 8, 8, FAKE, FAKE, None) == 1         # not an input type
+    assert f(st.BF16, None, 4, 8, 8, FAKE, FAKE, None) == 1        # null W
+    assert f(st.BF16, FAKE, 4, 8, 4, FAKE, FAKE, None) == 1        # ldw < K
+    assert f(st.BF16, FAKE, -1, 8, 8, FAKE, FAKE, None) == 1       # negative M
+    assert f(st.BF16, None, 0, 8, 8, None, None, None) == 0        # empty: no-op
+    assert lib.st24_decompress(st.E4M3, FAKE, None, 4, 8, FAKE, 8, None) == 1
+
+
+def test_spmm_rejects_bad_arguments(lib):
+    f = lib.st24_spmm
+
+    def call(ab=st.BF16, c=st.BF16, M=128, N=8, K=256, alpha=1.0, beta=0.0, v=FAKE, e=FAKE, B=FAKE,
+             ldb=256, C=FAKE, ldc=128, scale=None):
+        return f(ab, c, M, N, K, alpha, v, e, B, ldb, beta, C, ldc, scale, None, 0, None)
+
+    assert call(K=130) == 1                              # K % 4
+    assert call(K=132) == 2                              # K % 128: unsupported
+    assert call(c=st.S32) == 2                           # int32 out needs int8 in
+    assert call(ab=st.S8, c=st.S32, alpha=2.0) == 2      # int32 out: plain sums only
+    assert call(ab=st.F32) == 1
+    assert call(v=None) == 1
+    assert call(ldb=128) == 1                            # ldb < K
+    assert call(ldc=64) == 1                             # ldc < M
+    assert call(v=FAKE + 8) == 3                         # A values not 16-byte aligned
+    assert call(ldb=260) == 3                            # ldb * 2 bytes not a multiple of 16
+    assert call(C=FAKE + 1) == 3                         # C not aligned to its element
+    assert call(M=0, v=None, e=None, B=None, C=None) == 0    # empty: no-op

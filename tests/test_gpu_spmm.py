@@ -1,0 +1,153 @@
+"""SpMM on the GPU against the oracle, element by element.
+
+Small and ragged shapes are compared in full; the full-size workloads are
+compared on sampled outputs the oracle computes one by one, plus properties
+that hold at any size (determinism, workspace reuse)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import st24_inputs as inputs
+import structured_sparse_gemm_gb300 as st
+from helpers import assert_close, bits, decode_out
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def gpu_run(case, out=None, repeat=1, ws=None):
+    """Prune+compress A and run the product on the GPU through the C ABI."""
+    Ad = case.A.to(DEV)
+    values, meta = st.compress(Ad)
+    X = case.X.to(DEV)
+    tdt = inputs.TORCH_DTYPE[case.c]
+    outs = []
+    for _ in range(repeat):
+        Y = case.C_in.to(DEV).to(tdt) if case.C_in is not None else torch.full(
+            (case.N, case.M), 3, dtype=torch.int32 if case.c == "s32" else torch.float32, device=DEV).to(tdt)
+        scale = case.scale.to(DEV) if case.scale is not None else None
+        wsz = st.st24_spmm_workspace_bytes(case.ab, case.c, case.M, case.N, case.K)
+        w = ws if ws is not None else (torch.zeros(max(wsz, 1), dtype=torch.uint8, device=DEV) if wsz else None)
+        st.st24_spmm(values, meta, X, Y, K=case.K, alpha=case.alpha, beta=case.beta, row_scale=scale, workspace=w)
+        torch.cuda.synchronize()
+        outs.append(Y)
+    assert st.st24_device_status() == 0
+    return values, meta, outs
+
+
+def oracle_full(case):
+    _, _, ov, om = oracle.prune_compress(case.ab, bits(case.A))
+    Cin = bits(case.C_in.to(inputs.TORCH_DTYPE[case.c])) if case.C_in is not None else None
+    out, acc = oracle.spmm(case.ab, case.c, ov, om, bits(case.X), case.K, alpha=case.alpha, beta=case.beta,
+                           C_in=Cin, scale=None if case.scale is None else case.scale.numpy())
+    return (acc.astype(np.float64) if case.c == "s32" else out)
+
+
+def check_full(case):
+    _, _, (Y,) = gpu_run(case)
+    assert_close(decode_out(Y), oracle_full(case), case.ab, case.c, case.name)
+
+
+def sample_points(M, N, count, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = list(rng.integers(0, M, count)) + [0, M - 1, min(127, M - 1), min(128, M - 1)] * 2
+    cols = list(rng.integers(0, N, count)) + [0, N - 1] * 4
+    return np.array(rows, np.int64), np.array(cols, np.int64)
+
+
+def check_sampled(case, count=2048):
+    values, meta, (Y,) = gpu_run(case)
+    rows, cols = sample_points(case.M, case.N, count)
+    # the oracle samples from its own compressed form of the same input
+    _, _, ov, om = oracle.prune_compress(case.ab, bits(case.A))
+    Cin = bits(case.C_in.to(inputs.TORCH_DTYPE[case.c])) if case.C_in is not None else None
+    ref, acc = oracle.spmm_sampled(case.ab, case.c, ov, om, bits(case.X), case.K, rows, cols, alpha=case.alpha,
+                                   beta=case.beta, C_in=Cin,
+                                   scale=None if case.scale is None else case.scale.numpy())
+    got = decode_out(Y)[cols, rows]
+    full_scale = decode_out(Y)
+    assert_close(got, acc.astype(np.float64) if case.c == "s32" else ref, case.ab, case.c, case.name)
+    assert np.isfinite(full_scale).all()
+    # and the GPU's compressed form is the oracle's
+    assert np.array_equal(bits(values).view(np.uint8), ov.view(np.uint8))
+    assert np.array_equal(meta.cpu().numpy(), om)
+
+
+# ---- small / ragged shapes, compared in full ------------------------------------
+
+def test_small_f16_workload():
+    check_full(inputs.small_f16())
+
+
+@pytest.mark.parametrize("ab", ["f16", "bf16", "e4m3", "s8"])
+@pytest.mark.parametrize("c", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", [(200, 37, 384), (129, 1, 128), (64, 130, 512), (300, 64, 256)])
+def test_ragged(ab, c, M, N, K):
+    case = inputs.spmm_case(ab, c, M, N, K, a_std=0.02 if ab == "e4m3" else 1.0, seed=M + N + K)
+    check_full(case)
+
+
+@pytest.mark.parametrize("ab", ["f16", "bf16", "e4m3", "s8"])
+def test_alpha_beta_scale(ab):
+    case = inputs.spmm_case(ab, "bf16", 257, 48, 640, alpha=0.5, beta=-0.75, with_scale=True,
+                            a_std=0.02 if ab == "e4m3" else 1.0, seed=11)
+    check_full(case)
+
+
+@pytest.mark.parametrize("N", [8, 200])
+def test_int8_int32_bit_exact(N):
+    case = inputs.spmm_case("s8", "s32", 384, N, 1024, seed=N)
+    check_full(case)
+
+
+def test_k_equals_zero():
+    Y = torch.randn(5, 7, device=DEV)
+    Y0 = Y.clone()
+    X = torch.empty((5, 0), dtype=torch.bfloat16, device=DEV)
+    v = torch.empty((7, 0), dtype=torch.bfloat16, device=DEV)
+    e = torch.empty((7, 0), dtype=torch.uint8, device=DEV)
+    st.st24_spmm(v, e, X, Y, K=0, beta=2.0)
+    torch.cuda.synchronize()
+    assert torch.equal(Y, 2.0 * Y0)
+
+
+def test_deterministic_and_workspace_reuse():
+    case = inputs.decode_bf16(32)
+    wsz = st.st24_spmm_workspace_bytes("bf16", "bf16", case.M, case.N, case.K)
+    assert wsz > 0   # decode shapes are split over K
+    ws = torch.zeros(wsz, dtype=torch.uint8, device=DEV)
+    _, _, outs = gpu_run(case, repeat=3, ws=ws)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    # the per-tile counters (the workspace's last bytes) are back at zero after each call
+    assert int(ws[-256:].sum()) == 0
+
+
+# ---- the workloads at their full sizes -------------------------------------------
+
+@pytest.mark.parametrize("N", inputs.DECODE_NS)
+def test_decode_bf16_full(N):
+    check_full(inputs.decode_bf16(N))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("M,K", inputs.PREFILL_SHAPES)
+def test_prefill_bf16_sampled(M, K):
+    check_sampled(inputs.prefill_bf16(M, K))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("N", inputs.INT8_NS)
+def test_int8_sampled(N):
+    check_sampled(inputs.int8(N))
+
+
+@pytest.mark.slow
+def test_int8_int32_full_size_sampled():
+    check_sampled(inputs.int8(2048, out="s32"))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("N", inputs.FP8_NS)
+def test_fp8_sampled(N):
+    check_sampled(inputs.fp8(N), count=1024)
