@@ -77,6 +77,13 @@ typedef enum st24_status {
     ST24_ERR_WORKSPACE = 6      /* the workspace passed to st24_spmm is too small */
 } st24_status;
 
+/* Kernel families st24_spmm_ex can be asked to use. */
+typedef enum st24_kernel {
+    ST24_KERNEL_AUTO = 0,     /* what st24_spmm uses: TCGEN05 for f16/bf16/e4m3, MMA_SP for int8 */
+    ST24_KERNEL_TCGEN05 = 1,  /* tcgen05.mma.sp with TMEM accumulators (f16, bf16, e4m3 only) */
+    ST24_KERNEL_MMA_SP = 2    /* warp-level mma.sp (all input types) */
+} st24_kernel;
+
 /* Library version, (major << 16) | (minor << 8) | patch. */
 ST24_API int st24_version(void);
 
@@ -165,6 +172,19 @@ ST24_API st24_status st24_spmm(st24_dtype ab_type, st24_dtype c_type, int64_t M,
                       float alpha, const void* A_values, const void* A_meta,
                       const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
                       const float* row_scale, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * st24_spmm on an explicitly chosen kernel family (for testing one family
+ * against another, or a family against the oracle).  ST24_KERNEL_TCGEN05
+ * with ab_type ST24_S8 returns ST24_ERR_UNSUPPORTED.  Arguments, workspace
+ * and results are as for st24_spmm; st24_spmm_workspace_bytes covers every
+ * family.  An unknown `kernel` returns ST24_ERR_INVALID_ARG.
+ */
+ST24_API st24_status st24_spmm_ex(st24_kernel kernel, st24_dtype ab_type, st24_dtype c_type, int64_t M,
+                                  int64_t N, int64_t K, float alpha, const void* A_values,
+                                  const void* A_meta, const void* B, int64_t ldb, float beta, void* C,
+                                  int64_t ldc, const float* row_scale, void* workspace, size_t ws_bytes,
+                                  void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the status word the kernels

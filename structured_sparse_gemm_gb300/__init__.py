@@ -21,10 +21,12 @@ from . import _build_lib
 __all__ = [
     "St24Error", "load", "st24_version", "st24_status_string", "st24_values_bytes",
     "st24_meta_bytes", "st24_prune_compress", "st24_decompress", "st24_spmm_workspace_bytes",
-    "st24_spmm", "st24_device_status", "dtype_code", "compress", "spmm", "Workspace",
+    "st24_spmm", "st24_spmm_ex", "st24_device_status", "dtype_code", "compress", "spmm", "Workspace",
 ]
 
 F16, BF16, E4M3, S8, F32, S32 = 0, 1, 2, 3, 4, 5
+KERNEL_AUTO, KERNEL_TCGEN05, KERNEL_MMA_SP = 0, 1, 2
+_KERNELS = {"auto": KERNEL_AUTO, "tcgen05": KERNEL_TCGEN05, "mma_sp": KERNEL_MMA_SP}
 _TORCH_CODE = {
     torch.float16: F16, torch.bfloat16: BF16, torch.float8_e4m3fn: E4M3, torch.int8: S8,
     torch.float32: F32, torch.int32: S32,
@@ -65,6 +67,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.st24_spmm_workspace_bytes.restype = sz
     lib.st24_spmm.argtypes = [i, i, i64, i64, i64, f, p, p, p, i64, f, p, i64, p, p, sz, p]
     lib.st24_spmm.restype = i
+    lib.st24_spmm_ex.argtypes = [i, i, i, i64, i64, i64, f, p, p, p, i64, f, p, i64, p, p, sz, p]
+    lib.st24_spmm_ex.restype = i
     lib.st24_device_status.argtypes = [p]
     lib.st24_device_status.restype = i
     _lib = lib
@@ -140,17 +144,26 @@ def st24_spmm_workspace_bytes(ab, c, M: int, N: int, K: int) -> int:
 
 def st24_spmm(values: torch.Tensor, meta: torch.Tensor, X: torch.Tensor, Y: torch.Tensor, *, K: int | None = None,
               alpha: float = 1.0, beta: float = 0.0, row_scale: torch.Tensor | None = None,
-              workspace: torch.Tensor | None = None, M: int | None = None, stream=None) -> None:
-    """Y[N, M] = alpha * row_scale * (A_sparse @ X.T).T + beta * Y, A given by (values, meta)."""
+              workspace: torch.Tensor | None = None, M: int | None = None, stream=None,
+              kernel: str | int = "auto") -> None:
+    """Y[N, M] = alpha * row_scale * (A_sparse @ X.T).T + beta * Y, A given by (values, meta).
+
+    ``kernel`` picks the kernel family ("auto", "tcgen05" or "mma_sp"); anything
+    but "auto" goes through st24_spmm_ex."""
     N, Kx = X.shape
     K = Kx if K is None else K
     M = Y.shape[1] if M is None else M
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if X.stride(1) != 1 or Y.stride(1) != 1:
         raise ValueError("X and Y must have unit stride along their last dimension")
-    _check(load().st24_spmm(dtype_code(X.dtype), dtype_code(Y.dtype), M, N, K, float(alpha), _ptr(values),
-                            _ptr(meta), _ptr(X), X.stride(0), float(beta), _ptr(Y), Y.stride(0),
-                            _ptr(row_scale), _ptr(workspace), ws_bytes, _stream(stream)), "st24_spmm")
+    args = (dtype_code(X.dtype), dtype_code(Y.dtype), M, N, K, float(alpha), _ptr(values), _ptr(meta), _ptr(X),
+            X.stride(0), float(beta), _ptr(Y), Y.stride(0), _ptr(row_scale), _ptr(workspace), ws_bytes,
+            _stream(stream))
+    k = _KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
+    if k == KERNEL_AUTO:
+        _check(load().st24_spmm(*args), "st24_spmm")
+    else:
+        _check(load().st24_spmm_ex(k, *args), "st24_spmm_ex")
 
 
 def st24_device_status(stream=None) -> int:

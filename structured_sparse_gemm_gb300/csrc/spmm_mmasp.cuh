@@ -22,7 +22,7 @@
 //  * Consumer warps (4 x WARPS_N): ldmatrix fragments, mma.sp into registers.
 //  * Epilogue: alpha, per-row scale, beta * C, rounding to the output type.
 #pragma once
-#include "st24_device.cuh"
+#include "st24_epilogue.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -67,54 +67,13 @@ struct Config {
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
-struct Params {
-  int64_t M, N, K;
+struct Params : OutParams {
+  int64_t K;
   int64_t tiles_n, k_iters, total_iters;
-  float alpha, beta;
-  void* C;
-  int64_t ldc;
-  int c_type;
-  const float* row_scale;
   float* partials;       // [2 * gridDim.x][PARTIAL_ELEMS]
   unsigned* counters;    // one per output tile
   unsigned* status;
 };
-
-// ---- schedule helpers ---------------------------------------------------------
-__device__ __forceinline__ int64_t iter_begin(int64_t c, int64_t T, int64_t G) { return c * T / G; }
-// The CTA whose run contains iteration u.
-__device__ __forceinline__ int64_t iter_owner(int64_t u, int64_t T, int64_t G) {
-  return ((u + 1) * G - 1) / T;
-}
-
-// ---- output -------------------------------------------------------------------
-__device__ __forceinline__ float load_c(const Params& p, int64_t idx) {
-  switch (p.c_type) {
-    case kF32: return static_cast<const float*>(p.C)[idx];
-    case kBF16: return __bfloat162float(static_cast<const __nv_bfloat16*>(p.C)[idx]);
-    default: return __half2float(static_cast<const __half*>(p.C)[idx]);
-  }
-}
-
-template <typename Acc>
-__device__ __forceinline__ void store_out(const Params& p, int64_t m, int64_t n, Acc acc) {
-  const int64_t idx = n * p.ldc + m;
-  if constexpr (std::is_same<Acc, int>::value) {
-    if (p.c_type == kS32) {
-      static_cast<int*>(p.C)[idx] = acc;
-      return;
-    }
-  }
-  const float a = static_cast<float>(acc);
-  const float s = p.row_scale ? __fmul_rn(p.alpha, p.row_scale[m]) : p.alpha;
-  float r = __fmul_rn(a, s);
-  if (p.beta != 0.0f) r = __fadd_rn(r, __fmul_rn(p.beta, load_c(p, idx)));
-  switch (p.c_type) {
-    case kF32: static_cast<float*>(p.C)[idx] = r; break;
-    case kBF16: static_cast<__nv_bfloat16*>(p.C)[idx] = __float2bfloat16_rn(r); break;
-    default: static_cast<__half*>(p.C)[idx] = __float2half_rn(r); break;
-  }
-}
 
 __device__ __forceinline__ void consumer_sync(int threads) {
   asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
@@ -306,9 +265,7 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
       // Partial tile: publish it, and let the last contributor finish the tile.
       const int64_t c_lo = iter_owner(tile * KI, Ttot, G);
       const int64_t c_hi = iter_owner(tile * KI + KI - 1, Ttot, G);
-      auto slot_of = [&](int64_t c) -> int64_t {
-        return 2 * c + ((iter_begin(c, Ttot, G) / KI) == tile ? 0 : 1);
-      };
+      auto slot_of = [&](int64_t c) -> int64_t { return partial_slot(c, tile, Ttot, G, KI); };
       float4* mine = reinterpret_cast<float4*>(p.partials + slot_of(cta) * Cfg::PARTIAL_ELEMS);
 #pragma unroll
       for (int i = 0; i < 2; ++i)
@@ -337,35 +294,44 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
       consumer_sync(Cfg::CONSUMERS * 32);
       write_out = *s_last != 0;
       if (write_out) {
-        // Sum the partials in k order (segment c_lo first), one fragment at a
-        // time; this CTA's own partial is taken from its registers.
+        // Sum the partials in k order (segment c_lo first).  Each segment's
+        // fragments are loaded as one batch of independent loads, so a segment
+        // costs one memory latency; this CTA's own partial comes from registers.
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < 2; ++i) {
+          Acc t[WN][4];
+          for (int64_t c = c_lo; c <= c_hi; ++c) {
+            Acc v[WN][4];
+            if (c == cta) {
 #pragma unroll
-          for (int j = 0; j < WN; ++j) {
-            const int idx = ((warp * 2 + i) * WN + j) * 32 + lane;
-            Acc t[4];
-            for (int64_t c = c_lo; c <= c_hi; ++c) {
-              Acc v[4];
-              if (c == cta) {
+              for (int j = 0; j < WN; ++j)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) v[r] = acc[i][j][r];
-              } else {
-                const float4 f =
-                    __ldcg(reinterpret_cast<const float4*>(p.partials + slot_of(c) * Cfg::PARTIAL_ELEMS) + idx);
+                for (int r = 0; r < 4; ++r) v[j][r] = acc[i][j][r];
+            } else {
+              const float4* src = reinterpret_cast<const float4*>(p.partials + slot_of(c) * Cfg::PARTIAL_ELEMS);
+              float4 f[WN];
+#pragma unroll
+              for (int j = 0; j < WN; ++j) f[j] = __ldcg(src + ((warp * 2 + i) * WN + j) * 32 + lane);
+#pragma unroll
+              for (int j = 0; j < WN; ++j) {
                 if constexpr (T::kInt) {
-                  v[0] = __float_as_int(f.x); v[1] = __float_as_int(f.y);
-                  v[2] = __float_as_int(f.z); v[3] = __float_as_int(f.w);
+                  v[j][0] = __float_as_int(f[j].x); v[j][1] = __float_as_int(f[j].y);
+                  v[j][2] = __float_as_int(f[j].z); v[j][3] = __float_as_int(f[j].w);
                 } else {
-                  v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+                  v[j][0] = f[j].x; v[j][1] = f[j].y; v[j][2] = f[j].z; v[j][3] = f[j].w;
                 }
               }
-#pragma unroll
-              for (int r = 0; r < 4; ++r) t[r] = (c == c_lo) ? v[r] : t[r] + v[r];
             }
 #pragma unroll
-            for (int r = 0; r < 4; ++r) acc[i][j][r] = t[r];
+            for (int j = 0; j < WN; ++j)
+#pragma unroll
+              for (int r = 0; r < 4; ++r) t[j][r] = (c == c_lo) ? v[j][r] : t[j][r] + v[j][r];
           }
+#pragma unroll
+          for (int j = 0; j < WN; ++j)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[i][j][r] = t[j][r];
+        }
       }
     }
     if (write_out) {
@@ -377,7 +343,7 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
           for (int r = 0; r < 4; ++r) {
             const int64_t m = m_base + wm * 32 + i * 16 + gid + 8 * (r >> 1);
             const int64_t n = n_base + wn * WN * 8 + j * 8 + 2 * tig + (r & 1);
-            if (m < p.M && n < p.N) store_out<Acc>(p, m, n, acc[i][j][r]);
+            if (m < p.M && n < p.N) store_out<Acc>(p, m, n, acc[i][j][r], row_factor(p, m));
           }
     }
     it += kb1 - kb0;

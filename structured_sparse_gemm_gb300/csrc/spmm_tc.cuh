@@ -1,0 +1,414 @@
+// spmm_tc.cuh -- C = alpha * row_scale * (A_sparse * B) + beta * C on the
+// 5th-generation tensor cores (tcgen05.mma.sp), for f16, bf16 and fp8-e4m3.
+//
+// Method ("Chapter 26 -- Sparsity: The Hardware View", section "2:4
+// Fine-Grained Structured Sparsity"): each group's two stored weights multiply
+// the two activations its metadata selects; the sparse MMA reads the
+// compressed A (M x K/2) and a 4-bit-per-group metadata operand, so a 2:4 tile
+// costs half the multiply work of its dense shape.
+//
+// One persistent CTA per SM, 6 warps:
+//  * warp 0, TMA producer: per stage the compressed-A tile (128 rows x 128 B,
+//    128-byte swizzle), the B tile (BN rows x 256 B as two 128-byte swizzled
+//    boxes) and the metadata tile (128 rows x 16 B per box, no swizzle) into a
+//    ring of stages guarded by full/empty mbarriers.
+//  * warps 6-9, metadata: move the stage's metadata tile from shared memory
+//    into TMEM with tcgen05.st (each warp its 32-lane quadrant), in the order
+//    the sparse MMA reads it, and give rows past M a valid index pair.
+//  * warp 1, MMA issuer (one thread): issues 4 sparse MMAs per stage (M=128,
+//    N=BN, K=32 for 16-bit or 64 for 8-bit inputs) into a TMEM accumulator and
+//    commits the stage back to the producer.  Two accumulators alternate so
+//    the epilogue of a tile overlaps the next tile.  Warp 1 also owns the TMEM
+//    allocation.
+//  * warps 2-5, epilogue: tcgen05.ld of their 32-lane quadrant, then the fused
+//    alpha / row-scale / beta / rounding store; partial tiles of the stream-K
+//    schedule go through the workspace and are summed in k order by the last
+//    contributor.
+// Metadata order in TMEM (lane = row of the tile, one 32-bit column per 32
+// logical K of the MMA): for 8-bit inputs each column is the row's canonical
+// metadata word (8 groups, lowest K lowest).  For 16-bit inputs rows pair up
+// as (r, r+8) inside each 16-row block: lane r holds groups 0-3 of row r in
+// its low half and groups 0-3 of row r+8 in its high half, lane r+8 holds
+// groups 4-7 of the two rows the same way.
+#pragma once
+
+#include "st24_epilogue.cuh"
+
+namespace st24 {
+namespace tc {
+
+template <int DT>
+struct TcTraits {
+  static constexpr int ES = (DT == kF16 || DT == kBF16) ? 2 : 1;
+  static constexpr int KSTEP = 64 / ES;              // logical K per MMA
+  static constexpr int BK = 4 * KSTEP;               // logical K per stage
+  static constexpr int EB = BK / 8;                  // metadata bytes per row per stage
+  static constexpr int META_COLS_PER_MMA = KSTEP / 32;
+  static constexpr int META_COLS = EB / 4;           // TMEM columns of metadata per stage
+  static constexpr uint32_t FMT = (DT == kBF16) ? 1u : 0u;   // f16 0, bf16 1; e4m3 0 (kind::f8f6f4)
+};
+
+constexpr int pow2_at_least(int v) {
+  int p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+template <int DT, int BN_, int STAGES_>
+struct TcConfig {
+  using T = TcTraits<DT>;
+  static constexpr int BM = 128;
+  static constexpr int BN = BN_;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int THREADS = 320;
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 256;
+  static constexpr int E_BYTES = BM * T::EB;
+  static constexpr int STAGE_TX = A_BYTES + B_BYTES + E_BYTES;
+  static constexpr int STAGE_BYTES = (STAGE_TX + 1023) / 1024 * 1024;
+  static constexpr int META_COL0 = 2 * BN;           // after the two accumulators
+  static constexpr int TMEM_COLS = pow2_at_least(2 * BN + STAGES * T::META_COLS);
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int CH = BN < 32 ? BN : 32;       // columns per tcgen05.ld
+  // Instruction descriptor: sparse, fp32 accumulator, K-major A and B, N = BN, M = 128.
+  static constexpr uint32_t IDESC = (1u << 2) | (1u << 4) | (T::FMT << 7) | (T::FMT << 10) |
+                                    (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "N of the MMA");
+  static_assert(TMEM_COLS <= 512, "tensor memory");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+struct TcParams : OutParams {
+  int64_t K;
+  int64_t tiles_n, k_iters, total_iters;
+  float* partials;
+  unsigned* counters;
+  unsigned* status;
+};
+
+template <int DT, int BN, int STAGES>
+__global__ void __launch_bounds__(320, 1)
+    spmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmE,
+                   const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+  using Cfg = TcConfig<DT, BN, STAGES>;
+  using T = TcTraits<DT>;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* meta_bar = empty_bar + STAGES;      // [STAGES] metadata in TMEM
+  uint64_t* tfull_bar = meta_bar + STAGES;      // [2] accumulator ready
+  uint64_t* tempty_bar = tfull_bar + 2;         // [2] accumulator drained
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  int* s_last = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t G = gridDim.x, cta = blockIdx.x;
+  const int64_t Ttot = p.total_iters, KI = p.k_iters;
+  const int64_t it_begin = iter_begin(cta, Ttot, G), it_end = iter_begin(cta + 1, Ttot, G);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+      mbar_init(smem_u32(&meta_bar[s]), 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull_bar[b]), 1);
+      mbar_init(smem_u32(&tempty_bar[b]), 4);
+    }
+    mbar_init(smem_u32(drain_bar), 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmE);
+      tma_prefetch_desc(&tmB);
+      const uint64_t stream_once = policy_evict_first();
+      const uint64_t reuse = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_parity[STAGES];
+      bool issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = false;
+      bool ok = true;
+      for (int64_t it = it_begin; it < it_end && ok;) {
+        const int64_t tile = it / KI;
+        const int64_t kb0 = it - tile * KI;
+        const int64_t kb1 = min(KI, kb0 + (it_end - it));
+        const int32_t mt = static_cast<int32_t>(tile / p.tiles_n);
+        const int32_t nt = static_cast<int32_t>(tile - static_cast<int64_t>(mt) * p.tiles_n);
+        for (int64_t kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&full_bar[stage]);
+          mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
+          uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
+          const int32_t ka = static_cast<int32_t>(kb * (128 / T::ES));
+          const int32_t kB = static_cast<int32_t>(kb * T::BK);
+          tma_load_2d(smem_u32(st), &tmA, ka, mt * Cfg::BM, fb, stream_once);
+          tma_load_2d(smem_u32(st + Cfg::A_BYTES), &tmB, kB, nt * BN, fb, reuse);
+          tma_load_2d(smem_u32(st + Cfg::A_BYTES + BN * 128), &tmB, kB + 128 / T::ES, nt * BN, fb, reuse);
+          uint8_t* se = st + Cfg::A_BYTES + Cfg::B_BYTES;
+          const int32_t ke = static_cast<int32_t>(kb * T::EB);
+          tma_load_2d(smem_u32(se), &tmE, ke, mt * Cfg::BM, fb, stream_once);
+          if constexpr (T::EB == 32) tma_load_2d(smem_u32(se + 2048), &tmE, ke + 16, mt * Cfg::BM, fb, stream_once);
+          issued[stage] = true;
+          issued_parity[stage] = phase;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        it += kb1 - kb0;
+      }
+      // Never leave with copies in flight into this CTA's shared memory.
+      for (int s = 0; s < STAGES; ++s)
+        if (issued[s]) mbar_wait(smem_u32(&full_bar[s]), issued_parity[s], p.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int abuf = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      for (int64_t it = it_begin; it < it_end && ok;) {
+        const int64_t tile = it / KI;
+        const int64_t kb0 = it - tile * KI;
+        const int64_t kb1 = min(KI, kb0 + (it_end - it));
+        if (!mbar_wait(smem_u32(&tempty_bar[abuf]), aphase ^ 1u, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(abuf * BN);
+        for (int64_t kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(smem_u32(&meta_bar[stage]), phase, p.status) ||
+              !mbar_wait(smem_u32(&full_bar[stage]), phase, p.status)) { ok = false; break; }
+          tc_fence_after();
+          uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
+          const uint32_t mcol = tmem + static_cast<uint32_t>(Cfg::META_COL0 + stage * T::META_COLS);
+          const int64_t ks_left = (p.K - kb * T::BK) / T::KSTEP;
+          const int ksteps = ks_left < 4 ? static_cast<int>(ks_left) : 4;
+          const uint32_t a0 = smem_u32(st), b0 = smem_u32(st + Cfg::A_BYTES);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            if (ks >= ksteps) break;
+            const uint64_t da = smem_desc(a0 + ks * 32, 16, 1024, kSwizzle128B);
+            const uint64_t db = smem_desc(b0 + (ks >> 1) * (BN * 128) + (ks & 1) * 64, 16, 1024, kSwizzle128B);
+            const uint32_t acc = (kb > kb0 || ks > 0) ? 1u : 0u;
+            if constexpr (T::ES == 2)
+              tc_mma_sp_f16(d, da, db, mcol + ks * T::META_COLS_PER_MMA, Cfg::IDESC, acc);
+            else
+              tc_mma_sp_f8f6f4(d, da, db, mcol + ks * T::META_COLS_PER_MMA, Cfg::IDESC, acc);
+          }
+          tc_commit(smem_u32(&empty_bar[stage]));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&tfull_bar[abuf]));
+        if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
+        it += kb1 - kb0;
+      }
+      // Every tcgen05 operation of this thread has completed before TMEM is freed.
+      tc_commit(smem_u32(drain_bar));
+      mbar_wait(smem_u32(drain_bar), 0, p.status);
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ metadata
+    const int q = warp & 3;                 // TMEM lane quadrant of this warp
+    const int row = 32 * q + lane;          // row of the tile this lane moves
+    const uint4 fill = make_uint4(0x44444444u, 0x44444444u, 0x44444444u, 0x44444444u);  // index pair (0, 1)
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t it = it_begin; it < it_end && ok;) {
+      const int64_t tile = it / KI;
+      const int64_t kb0 = it - tile * KI;
+      const int64_t kb1 = min(KI, kb0 + (it_end - it));
+      const int64_t rows_valid = p.M - (tile / p.tiles_n) * Cfg::BM;   // rows past M hold zero-filled metadata
+      for (int64_t kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.status)) { ok = false; break; }
+        const uint8_t* se = smem + stage * Cfg::STAGE_BYTES + Cfg::A_BYTES + Cfg::B_BYTES;
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) +
+                               static_cast<uint32_t>(Cfg::META_COL0 + stage * T::META_COLS);
+        if constexpr (T::ES == 2) {
+          const int j = row & 15;
+          const int partner = j < 8 ? row + 8 : row - 8;
+          const uint4 own = row < rows_valid ? *reinterpret_cast<const uint4*>(se + row * 16) : fill;
+          const uint4 oth = partner < rows_valid ? *reinterpret_cast<const uint4*>(se + partner * 16) : fill;
+          const uint4 lo = j < 8 ? own : oth, hi = j < 8 ? oth : own;
+          const uint32_t sel = j < 8 ? 0x5410u : 0x7632u;
+          tmem_st_x4(taddr, __byte_perm(lo.x, hi.x, sel), __byte_perm(lo.y, hi.y, sel),
+                     __byte_perm(lo.z, hi.z, sel), __byte_perm(lo.w, hi.w, sel));
+        } else {
+          const bool in = row < rows_valid;
+          const uint4 a = in ? *reinterpret_cast<const uint4*>(se + row * 16) : fill;
+          const uint4 b = in ? *reinterpret_cast<const uint4*>(se + 2048 + row * 16) : fill;
+          tmem_st_x8(taddr, a, b);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&meta_bar[stage]));
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      it += kb1 - kb0;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                 // TMEM lane quadrant of this warp
+    int abuf = 0;
+    uint32_t aphase = 0;
+    constexpr int CH = Cfg::CH;
+    for (int64_t it = it_begin; it < it_end;) {
+      const int64_t tile = it / KI;
+      const int64_t kb0 = it - tile * KI;
+      const int64_t kb1 = min(KI, kb0 + (it_end - it));
+      const int64_t mt = tile / p.tiles_n, nt = tile - mt * p.tiles_n;
+      const int64_t m = mt * Cfg::BM + 32 * q + lane;
+      const int64_t n_base = nt * BN;
+      if (!mbar_wait(smem_u32(&tfull_bar[abuf]), aphase, p.status)) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(abuf * BN);
+      const bool whole = (kb0 == 0 && kb1 == KI);
+      const bool row_ok = m < p.M;
+      const float f = row_ok ? row_factor(p, m) : 0.0f;
+      if (whole) {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += CH) {
+          uint32_t r[CH];
+          if constexpr (CH == 32) tmem_ld_x32(tacc + c, r); else tmem_ld_x16(tacc + c, r);
+          tmem_ld_wait();
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+              const int64_t n = n_base + c + j;
+              if (n < p.N) store_out<float>(p, m, n, __uint_as_float(r[j]), f);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[abuf]));
+      } else {
+        float* mine = p.partials + partial_slot(cta, tile, Ttot, G, KI) * (Cfg::BM * BN);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += CH) {
+          uint32_t r[CH];
+          if constexpr (CH == 32) tmem_ld_x32(tacc + c, r); else tmem_ld_x16(tacc + c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < CH; ++j) __stcg(mine + (c + j) * Cfg::BM + 32 * q + lane, __uint_as_float(r[j]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[abuf]));
+        __threadfence();
+        named_barrier_sync(1, 128);
+        const int64_t c_lo = iter_owner(tile * KI, Ttot, G);
+        const int64_t c_hi = iter_owner(tile * KI + KI - 1, Ttot, G);
+        if (threadIdx.x == 64) {
+          const unsigned nseg = static_cast<unsigned>(c_hi - c_lo + 1);
+          const unsigned old = atomicAdd(p.counters + tile, 1u);
+          const int last = (old == nseg - 1) ? 1 : 0;
+          if (last) p.counters[tile] = 0;   // all contributors have arrived: ready for the next call
+          __threadfence();
+          *s_last = last;
+        }
+        named_barrier_sync(1, 128);
+        if (*s_last && row_ok) {
+          // Sum the partials in k order (segment c_lo first), CH columns at a
+          // time so each segment costs one batch of independent loads.
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += CH) {
+            float t[CH];
+            for (int64_t c = c_lo; c <= c_hi; ++c) {
+              const float* src = p.partials + partial_slot(c, tile, Ttot, G, KI) * (Cfg::BM * BN) + 32 * q + lane;
+              float v[CH];
+#pragma unroll
+              for (int j = 0; j < CH; ++j) v[j] = __ldcg(src + (c0 + j) * Cfg::BM);
+#pragma unroll
+              for (int j = 0; j < CH; ++j) t[j] = (c == c_lo) ? v[j] : t[j] + v[j];
+            }
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+              const int64_t n = n_base + c0 + j;
+              if (n < p.N) store_out<float>(p, m, n, t[j], f);
+            }
+          }
+        }
+      }
+      if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
+      it += kb1 - kb0;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, Cfg::TMEM_COLS);
+}
+
+template <int DT, int BN, int STAGES>
+st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev, cudaStream_t stream) {
+  using Cfg = TcConfig<DT, BN, STAGES>;
+  using T = TcTraits<DT>;
+  const CUtensorMapDataType ty = T::ES == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUtensorMap tmA, tmE, tmB;
+  const uint64_t kc = a.K / 2;
+  if (!encode_tensor_map_2d(&tmA, ty, a.values, kc, a.M, kc * T::ES, 128 / T::ES, Cfg::BM,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tensor_map_2d(&tmE, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.meta, a.K / 8, a.M, a.K / 8, 16, Cfg::BM,
+                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_tensor_map_2d(&tmB, ty, a.B, a.K, a.N, a.ldb * T::ES, 128 / T::ES, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return ST24_ERR_CUDA;
+  TcParams p{};
+  p.M = a.M; p.N = a.N; p.K = a.K;
+  p.alpha = a.alpha; p.beta = a.beta;
+  p.C = a.C; p.ldc = a.ldc; p.c_type = a.c;
+  p.row_scale = a.row_scale;
+  p.tiles_n = plan.tiles_n;
+  p.k_iters = plan.k_iters;
+  p.total_iters = plan.total_iters;
+  p.partials = static_cast<float*>(a.workspace);
+  p.counters = plan.ws_bytes ? reinterpret_cast<unsigned*>(static_cast<uint8_t*>(a.workspace) +
+                                                          2 * static_cast<size_t>(plan.grid) * plan.partial_bytes)
+                             : nullptr;
+  p.status = dev.status;
+  auto kern = spmm_tc_kernel<DT, BN, STAGES>;
+  static bool attr_set[64] = {};
+  if (!attr_set[dev.device % 64]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+      return ST24_ERR_CUDA;
+    attr_set[dev.device % 64] = true;
+  }
+  kern<<<plan.grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmE, tmB, p);
+  return cudaGetLastError() == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;
+}
+
+template <int DT>
+st24_status launch_dt_impl(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev, cudaStream_t s) {
+  constexpr bool k16 = TcTraits<DT>::ES == 2;
+  switch (plan.bn) {
+    case 16: return launch_cfg<DT, 16, 8>(a, plan, dev, s);
+    case 32: return launch_cfg<DT, 32, 7>(a, plan, dev, s);
+    case 64: return launch_cfg<DT, 64, k16 ? 6 : 6>(a, plan, dev, s);
+    default: return launch_cfg<DT, 128, 4>(a, plan, dev, s);
+  }
+}
+
+// Entry per element type (one translation unit each: spmm_tc_<type>.cu).
+template <int DT>
+st24_status launch_dt(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev, cudaStream_t s);
+
+}  // namespace tc
+}  // namespace st24

@@ -72,9 +72,45 @@ bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, const void
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+StreamKPlan make_stream_k_plan(int bm, int bn, int bk, int64_t M, int64_t N, int64_t K, int num_sms) {
+  StreamKPlan pl{};
+  pl.bm = bm;
+  pl.bn = bn;
+  pl.bk = bk;
+  pl.tiles_m = (M + bm - 1) / bm;
+  pl.tiles_n = (N + bn - 1) / bn;
+  pl.k_iters = (K + bk - 1) / bk;
+  pl.total_iters = pl.tiles_m * pl.tiles_n * pl.k_iters;
+  const int64_t grid = pl.total_iters < num_sms ? pl.total_iters : num_sms;
+  pl.grid = static_cast<int>(grid > 0 ? grid : 1);
+  pl.partial_bytes = static_cast<size_t>(bm) * bn * 4;
+  // Is any tile split between CTAs?  (CTA c starts at iteration c*T/G.)
+  bool split = false;
+  for (int64_t c = 1; c < pl.grid && !split; ++c)
+    if ((c * pl.total_iters / pl.grid) % pl.k_iters != 0) split = true;
+  const size_t tiles = static_cast<size_t>(pl.tiles_m * pl.tiles_n);
+  pl.ws_bytes = split ? 2 * static_cast<size_t>(pl.grid) * pl.partial_bytes + (tiles * 4 + 255) / 256 * 256 : 0;
+  return pl;
+}
+
 }  // namespace st24
 
 using namespace st24;
+
+namespace {
+
+// The kernel family a call runs on: tcgen05 for the 16-bit and fp8 inputs,
+// the warp-level sparse MMA for int8 (there is no int8 tcgen05 kind on sm_103a).
+int resolve_kernel(int requested, int ab) {
+  if (requested == ST24_KERNEL_AUTO) return ab == kS8 ? ST24_KERNEL_MMA_SP : ST24_KERNEL_TCGEN05;
+  return requested;
+}
+
+StreamKPlan plan_for(int kernel, const SpmmArgs& a, int num_sms) {
+  return kernel == ST24_KERNEL_TCGEN05 ? plan_spmm_tc(a, num_sms) : plan_spmm_mmasp(a, num_sms);
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -150,13 +186,21 @@ size_t st24_spmm_workspace_bytes(st24_dtype ab_type, st24_dtype c_type, int64_t 
   a.M = M;
   a.N = N;
   a.K = K;
-  return plan_spmm_mmasp(a, dev->num_sms).ws_bytes;
+  // Enough for whichever kernel family a call with these sizes may run on.
+  size_t ws = plan_spmm_mmasp(a, dev->num_sms).ws_bytes;
+  if (ab_type != ST24_S8) {
+    const size_t t = plan_spmm_tc(a, dev->num_sms).ws_bytes;
+    ws = t > ws ? t : ws;
+  }
+  return ws;
 }
 
-st24_status st24_spmm(st24_dtype ab_type, st24_dtype c_type, int64_t M, int64_t N, int64_t K,
-                      float alpha, const void* A_values, const void* A_meta, const void* B,
-                      int64_t ldb, float beta, void* C, int64_t ldc, const float* row_scale,
-                      void* workspace, size_t ws_bytes, void* stream) {
+st24_status st24_spmm_ex(st24_kernel kernel, st24_dtype ab_type, st24_dtype c_type, int64_t M, int64_t N,
+                         int64_t K, float alpha, const void* A_values, const void* A_meta, const void* B,
+                         int64_t ldb, float beta, void* C, int64_t ldc, const float* row_scale,
+                         void* workspace, size_t ws_bytes, void* stream) {
+  if (kernel != ST24_KERNEL_AUTO && kernel != ST24_KERNEL_TCGEN05 && kernel != ST24_KERNEL_MMA_SP)
+    return ST24_ERR_INVALID_ARG;
   SpmmArgs a{};
   a.ab = ab_type;
   a.c = c_type;
@@ -176,12 +220,24 @@ st24_status st24_spmm(st24_dtype ab_type, st24_dtype c_type, int64_t M, int64_t 
   a.ws_bytes = ws_bytes;
   st24_status st = check_spmm(a);
   if (st != ST24_OK || M == 0 || N == 0) return st;
+  const int k = resolve_kernel(kernel, ab_type);
+  if (k == ST24_KERNEL_TCGEN05 && ab_type == ST24_S8) return ST24_ERR_UNSUPPORTED;
   const DeviceInfo* dev = current_device_info();
   if (!dev) return ST24_ERR_CUDA;
-  const StreamKPlan plan = plan_spmm_mmasp(a, dev->num_sms);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return launch_scale_c(a, *dev, s);
+  const StreamKPlan plan = plan_for(k, a, dev->num_sms);
   if (plan.ws_bytes > 0 && (!workspace || ws_bytes < plan.ws_bytes || !aligned(workspace, 16)))
     return ST24_ERR_WORKSPACE;
-  return launch_spmm_mmasp(a, plan, *dev, static_cast<cudaStream_t>(stream));
+  return k == ST24_KERNEL_TCGEN05 ? launch_spmm_tc(a, plan, *dev, s) : launch_spmm_mmasp(a, plan, *dev, s);
+}
+
+st24_status st24_spmm(st24_dtype ab_type, st24_dtype c_type, int64_t M, int64_t N, int64_t K,
+                      float alpha, const void* A_values, const void* A_meta, const void* B,
+                      int64_t ldb, float beta, void* C, int64_t ldc, const float* row_scale,
+                      void* workspace, size_t ws_bytes, void* stream) {
+  return st24_spmm_ex(ST24_KERNEL_AUTO, ab_type, c_type, M, N, K, alpha, A_values, A_meta, B, ldb, beta, C, ldc,
+                      row_scale, workspace, ws_bytes, stream);
 }
 
 st24_status st24_device_status(void* stream) {

@@ -1,0 +1,74 @@
+// st24_epilogue.cuh -- the SpMM output stage shared by the kernels:
+// out(m, n) = round(alpha * row_scale[m] * acc + beta * C(m, n)), with C
+// element (m, n) at C[n*ldc + m].  The fp32 operations are done in this fixed
+// order without contraction, so every kernel rounds the same way.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+#include "st24_device.cuh"
+
+namespace st24 {
+
+struct OutParams {
+  int64_t M, N;
+  float alpha, beta;
+  void* C;
+  int64_t ldc;
+  int c_type;
+  const float* row_scale;
+};
+
+__device__ __forceinline__ float load_c(const OutParams& p, int64_t idx) {
+  switch (p.c_type) {
+    case kF32: return static_cast<const float*>(p.C)[idx];
+    case kBF16: return __bfloat162float(static_cast<const __nv_bfloat16*>(p.C)[idx]);
+    default: return __half2float(static_cast<const __half*>(p.C)[idx]);
+  }
+}
+
+// Row factor alpha * row_scale[m] (alpha when there is no scale).
+__device__ __forceinline__ float row_factor(const OutParams& p, int64_t m) {
+  return p.row_scale ? __fmul_rn(p.alpha, p.row_scale[m]) : p.alpha;
+}
+
+template <typename Acc>
+__device__ __forceinline__ void store_out(const OutParams& p, int64_t m, int64_t n, Acc acc, float factor) {
+  const int64_t idx = n * p.ldc + m;
+  if constexpr (std::is_same<Acc, int>::value) {
+    if (p.c_type == kS32) {
+      static_cast<int*>(p.C)[idx] = acc;
+      return;
+    }
+  }
+  float r = __fmul_rn(static_cast<float>(acc), factor);
+  if (p.beta != 0.0f) r = __fadd_rn(r, __fmul_rn(p.beta, load_c(p, idx)));
+  switch (p.c_type) {
+    case kF32: static_cast<float*>(p.C)[idx] = r; break;
+    case kBF16: static_cast<__nv_bfloat16*>(p.C)[idx] = __float2bfloat16_rn(r); break;
+    default: static_cast<__half*>(p.C)[idx] = __float2half_rn(r); break;
+  }
+}
+
+// C = beta * C over the whole M x N output (the product is empty when K == 0).
+__global__ void scale_c_kernel(OutParams p);
+
+// ---- stream-K schedule (shared by the persistent kernels) -------------------
+// Iterations (tile, k-block) are numbered tile * k_iters + kb; CTA c of G runs
+// [c*T/G, (c+1)*T/G).
+__device__ __forceinline__ int64_t iter_begin(int64_t c, int64_t T, int64_t G) { return c * T / G; }
+// The CTA whose run contains iteration u.
+__device__ __forceinline__ int64_t iter_owner(int64_t u, int64_t T, int64_t G) {
+  return ((u + 1) * G - 1) / T;
+}
+// Workspace slot of CTA c's partial of `tile`: 2c for the first tile of its run,
+// 2c + 1 for the last (a run has at most these two partial tiles).
+__device__ __forceinline__ int64_t partial_slot(int64_t c, int64_t tile, int64_t T, int64_t G,
+                                                int64_t k_iters) {
+  return 2 * c + ((iter_begin(c, T, G) / k_iters) == tile ? 0 : 1);
+}
+
+}  // namespace st24

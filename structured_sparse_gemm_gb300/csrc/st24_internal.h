@@ -72,10 +72,20 @@ struct StreamKPlan {
   size_t ws_bytes;         // workspace bytes (0 if no tile is split)
 };
 
+// A stream-K plan over a persistent grid of at most num_sms CTAs.
+StreamKPlan make_stream_k_plan(int bm, int bn, int bk, int64_t M, int64_t N, int64_t K, int num_sms);
+
 // The mma.sp (warp-level sparse MMA) path: every element type.
 StreamKPlan plan_spmm_mmasp(const SpmmArgs& a, int num_sms);
 st24_status launch_spmm_mmasp(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev,
                               cudaStream_t stream);
+
+// The tcgen05 (5th-generation tensor core) path: f16, bf16, e4m3.
+StreamKPlan plan_spmm_tc(const SpmmArgs& a, int num_sms);
+st24_status launch_spmm_tc(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev,
+                           cudaStream_t stream);
+// C = beta * C when K == 0.
+st24_status launch_scale_c(const SpmmArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
 // Tensor maps (driver entry point fetched through the runtime, so the library
 // has no link-time dependency on libcuda).

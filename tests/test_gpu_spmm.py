@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-def gpu_run(case, out=None, repeat=1, ws=None):
+def gpu_run(case, out=None, repeat=1, ws=None, kernel="auto"):
     """Prune+compress A and run the product on the GPU through the C ABI."""
     Ad = case.A.to(DEV)
     values, meta = st.compress(Ad)
@@ -29,7 +29,8 @@ def gpu_run(case, out=None, repeat=1, ws=None):
         scale = case.scale.to(DEV) if case.scale is not None else None
         wsz = st.st24_spmm_workspace_bytes(case.ab, case.c, case.M, case.N, case.K)
         w = ws if ws is not None else (torch.zeros(max(wsz, 1), dtype=torch.uint8, device=DEV) if wsz else None)
-        st.st24_spmm(values, meta, X, Y, K=case.K, alpha=case.alpha, beta=case.beta, row_scale=scale, workspace=w)
+        st.st24_spmm(values, meta, X, Y, K=case.K, alpha=case.alpha, beta=case.beta, row_scale=scale, workspace=w,
+                     kernel=kernel)
         torch.cuda.synchronize()
         outs.append(Y)
     assert st.st24_device_status() == 0
@@ -44,8 +45,8 @@ def oracle_full(case):
     return (acc.astype(np.float64) if case.c == "s32" else out)
 
 
-def check_full(case):
-    _, _, (Y,) = gpu_run(case)
+def check_full(case, kernel="auto"):
+    _, _, (Y,) = gpu_run(case, kernel=kernel)
     assert_close(decode_out(Y), oracle_full(case), case.ab, case.c, case.name)
 
 
@@ -56,8 +57,8 @@ def sample_points(M, N, count, seed=0):
     return np.array(rows, np.int64), np.array(cols, np.int64)
 
 
-def check_sampled(case, count=2048):
-    values, meta, (Y,) = gpu_run(case)
+def check_sampled(case, count=2048, kernel="auto"):
+    values, meta, (Y,) = gpu_run(case, kernel=kernel)
     rows, cols = sample_points(case.M, case.N, count)
     # the oracle samples from its own compressed form of the same input
     _, _, ov, om = oracle.prune_compress(case.ab, bits(case.A))
@@ -76,23 +77,39 @@ def check_sampled(case, count=2048):
 
 # ---- small / ragged shapes, compared in full ------------------------------------
 
-def test_small_f16_workload():
-    check_full(inputs.small_f16())
+KERNELS = ["tcgen05", "mma_sp"]
 
 
+def kernels_for(ab):
+    return ["mma_sp"] if ab == "s8" else KERNELS
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_small_f16_workload(kernel):
+    check_full(inputs.small_f16(), kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("ab", ["f16", "bf16", "e4m3", "s8"])
 @pytest.mark.parametrize("c", ["f32", "bf16", "f16"])
-@pytest.mark.parametrize("M,N,K", [(200, 37, 384), (129, 1, 128), (64, 130, 512), (300, 64, 256)])
-def test_ragged(ab, c, M, N, K):
-    case = inputs.spmm_case(ab, c, M, N, K, a_std=0.02 if ab == "e4m3" else 1.0, seed=M + N + K)
-    check_full(case)
+@pytest.mark.parametrize("M,N,K", [(200, 37, 384), (129, 1, 128), (64, 130, 512), (300, 64, 256), (384, 200, 1280)])
+def test_ragged(kernel, ab, c, M, N, K):
+    if kernel not in kernels_for(ab):
+        pytest.skip("no int8 tcgen05 kind on sm_103a")
+    # int8 sums reach ~1e5 and overflow f16 unless scaled, as the int8 workload is (1/127 per row)
+    case = inputs.spmm_case(ab, c, M, N, K, a_std=0.02 if ab == "e4m3" else 1.0, seed=M + N + K,
+                            with_scale=(ab == "s8"))
+    check_full(case, kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("ab", ["f16", "bf16", "e4m3", "s8"])
-def test_alpha_beta_scale(ab):
+def test_alpha_beta_scale(kernel, ab):
+    if kernel not in kernels_for(ab):
+        pytest.skip("no int8 tcgen05 kind on sm_103a")
     case = inputs.spmm_case(ab, "bf16", 257, 48, 640, alpha=0.5, beta=-0.75, with_scale=True,
                             a_std=0.02 if ab == "e4m3" else 1.0, seed=11)
-    check_full(case)
+    check_full(case, kernel=kernel)
 
 
 @pytest.mark.parametrize("N", [8, 200])
@@ -125,9 +142,27 @@ def test_deterministic_and_workspace_reuse():
 
 # ---- the workloads at their full sizes -------------------------------------------
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("N", inputs.DECODE_NS)
-def test_decode_bf16_full(N):
-    check_full(inputs.decode_bf16(N))
+def test_decode_bf16_full(kernel, N):
+    check_full(inputs.decode_bf16(N), kernel=kernel)
+
+
+def test_kernel_families_agree():
+    # the two kernel families compute the same sums; on one k-block per tile they agree closely
+    case = inputs.spmm_case("bf16", "f32", 512, 96, 2048, seed=5)
+    _, _, (Ya,) = gpu_run(case, kernel="tcgen05")
+    _, _, (Yb,) = gpu_run(case, kernel="mma_sp")
+    ref = oracle_full(case)
+    assert_close(decode_out(Ya), ref, "bf16", "f32", "tcgen05")
+    assert_close(decode_out(Yb), ref, "bf16", "f32", "mma_sp")
+
+
+def test_tcgen05_rejects_int8():
+    case = inputs.spmm_case("s8", "s32", 128, 16, 256, seed=1)
+    with pytest.raises(st.St24Error) as e:
+        gpu_run(case, kernel="tcgen05")
+    assert e.value.status == 2
 
 
 @pytest.mark.slow
@@ -151,3 +186,14 @@ def test_int8_int32_full_size_sampled():
 @pytest.mark.parametrize("N", inputs.FP8_NS)
 def test_fp8_sampled(N):
     check_sampled(inputs.fp8(N), count=1024)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("N", [64, 4096])
+def test_fp8_sampled_mma_sp(N):
+    check_sampled(inputs.fp8(N), count=512, kernel="mma_sp")
+
+
+@pytest.mark.slow
+def test_prefill_bf16_sampled_mma_sp():
+    check_sampled(inputs.prefill_bf16(4096, 11008), count=512, kernel="mma_sp")
