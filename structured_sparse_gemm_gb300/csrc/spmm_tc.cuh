@@ -25,8 +25,9 @@
 //    schedule go through the workspace and are summed in k order by the last
 //    contributor.
 // Metadata order in TMEM (lane = row of the tile, one 32-bit column per 32
-// logical K of the MMA): for 8-bit inputs each column is the row's canonical
-// metadata word (8 groups, lowest K lowest).  For 16-bit inputs rows pair up
+// logical K of an MMA, the columns of each MMA starting on a 4-column
+// boundary): for 8-bit inputs each column is the row's canonical metadata word
+// (8 groups, lowest K lowest).  For 16-bit inputs rows pair up
 // as (r, r+8) inside each 16-row block: lane r holds groups 0-3 of row r in
 // its low half and groups 0-3 of row r+8 in its high half, lane r+8 holds
 // groups 4-7 of the two rows the same way.
@@ -43,8 +44,11 @@ struct TcTraits {
   static constexpr int KSTEP = 64 / ES;              // logical K per MMA
   static constexpr int BK = 4 * KSTEP;               // logical K per stage
   static constexpr int EB = BK / 8;                  // metadata bytes per row per stage
+  // Metadata of MMA ks of a stage sits at column 4*ks of the stage's 16-column
+  // slot (4-column aligned, read with sparsity selector 0): one column for
+  // 16-bit inputs, two for 8-bit inputs.
   static constexpr int META_COLS_PER_MMA = KSTEP / 32;
-  static constexpr int META_COLS = EB / 4;           // TMEM columns of metadata per stage
+  static constexpr int META_COLS = 16;               // TMEM columns of metadata per stage
   static constexpr uint32_t FMT = (DT == kBF16) ? 1u : 0u;   // f16 0, bf16 1; e4m3 0 (kind::f8f6f4)
 };
 
@@ -206,9 +210,9 @@ __global__ void __launch_bounds__(320, 1)
             const uint64_t db = smem_desc(b0 + (ks >> 1) * (BN * 128) + (ks & 1) * 64, 16, 1024, kSwizzle128B);
             const uint32_t acc = (kb > kb0 || ks > 0) ? 1u : 0u;
             if constexpr (T::ES == 2)
-              tc_mma_sp_f16(d, da, db, mcol + ks * T::META_COLS_PER_MMA, Cfg::IDESC, acc);
+              tc_mma_sp_f16(d, da, db, mcol + 4 * ks, Cfg::IDESC, acc);
             else
-              tc_mma_sp_f8f6f4(d, da, db, mcol + ks * T::META_COLS_PER_MMA, Cfg::IDESC, acc);
+              tc_mma_sp_f8f6f4(d, da, db, mcol + 4 * ks, Cfg::IDESC, acc);
           }
           tc_commit(smem_u32(&empty_bar[stage]));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -240,6 +244,9 @@ __global__ void __launch_bounds__(320, 1)
         const uint8_t* se = smem + stage * Cfg::STAGE_BYTES + Cfg::A_BYTES + Cfg::B_BYTES;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) +
                                static_cast<uint32_t>(Cfg::META_COL0 + stage * T::META_COLS);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = fill.x;
         if constexpr (T::ES == 2) {
           const int j = row & 15;
           const int partner = j < 8 ? row + 8 : row - 8;
@@ -247,14 +254,18 @@ __global__ void __launch_bounds__(320, 1)
           const uint4 oth = partner < rows_valid ? *reinterpret_cast<const uint4*>(se + partner * 16) : fill;
           const uint4 lo = j < 8 ? own : oth, hi = j < 8 ? oth : own;
           const uint32_t sel = j < 8 ? 0x5410u : 0x7632u;
-          tmem_st_x4(taddr, __byte_perm(lo.x, hi.x, sel), __byte_perm(lo.y, hi.y, sel),
-                     __byte_perm(lo.z, hi.z, sel), __byte_perm(lo.w, hi.w, sel));
+          w[0] = __byte_perm(lo.x, hi.x, sel);
+          w[4] = __byte_perm(lo.y, hi.y, sel);
+          w[8] = __byte_perm(lo.z, hi.z, sel);
+          w[12] = __byte_perm(lo.w, hi.w, sel);
         } else {
           const bool in = row < rows_valid;
           const uint4 a = in ? *reinterpret_cast<const uint4*>(se + row * 16) : fill;
           const uint4 b = in ? *reinterpret_cast<const uint4*>(se + 2048 + row * 16) : fill;
-          tmem_st_x8(taddr, a, b);
+          w[0] = a.x; w[1] = a.y; w[4] = a.z; w[5] = a.w;
+          w[8] = b.x; w[9] = b.y; w[12] = b.z; w[13] = b.w;
         }
+        tmem_st_x16(taddr, w);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
