@@ -45,7 +45,7 @@ WORKLOADS = {
                  desc="int8 2:4 SpMM: 8192x8192 weights uniform [-127,127], N in {16,2048}, int32 accumulate, "
                       "per-row fp32 scale, bf16 out"),
     "fp8": dict(ab="e4m3", c="bf16", shapes=[(28672, 8192)], Ns=list(inputs.FP8_NS), layers=1, a_std=0.02,
-                beta=0.0, scale=False,
+                beta=0.0, scale=False, extra_prune_bf16=(28672, 8192),
                 desc="fp8-e4m3 2:4 SpMM: 28672x8192 weights N(0,0.02), N in {1,64,512,4096,8192}, bf16 out"),
 }
 
@@ -174,13 +174,13 @@ def prune_phase(layers, stream=None):
         st.st24_prune_compress(L["A"], L["values"], L["meta"], stream=stream)
 
 
-def spmm_phase(layers, w, stream=None):
+def spmm_phase(layers, w, stream=None, kernel="auto"):
     import structured_sparse_gemm_gb300 as st
     for ni in range(len(w["Ns"])):
         for L in layers:
             X, Y, ws = L["acts"][ni]
             st.st24_spmm(L["values"], L["meta"], X, Y, K=L["K"], beta=w["beta"], row_scale=L["scale"],
-                         workspace=ws, stream=stream)
+                         workspace=ws, stream=stream, kernel=kernel)
 
 
 def run_gpu(args, w, rank, world):
@@ -194,13 +194,13 @@ def run_gpu(args, w, rank, world):
     with torch.cuda.stream(stream):
         # eager warm-up (also sets kernel attributes before capture)
         prune_phase(layers)
-        spmm_phase(layers, w)
+        spmm_phase(layers, w, kernel=args.kernel)
         stream.synchronize()
         g_prune, g_spmm = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_prune, stream=stream):
             prune_phase(layers)
         with torch.cuda.graph(g_spmm, stream=stream):
-            spmm_phase(layers, w)
+            spmm_phase(layers, w, kernel=args.kernel)
     for _ in range(args.warmup):
         g_prune.replay()
         g_spmm.replay()
@@ -223,13 +223,34 @@ def run_gpu(args, w, rank, world):
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
+    extra = None
+    if w.get("extra_prune_bf16"):
+        # prune/compress of the bf16 weight the fp8 one is cast from (timed apart from the step)
+        M, K = w["extra_prune_bf16"]
+        Wb = inputs.prune_weight_bf16(M, K).to(layers[0]["A"].device)
+        vb = torch.empty((M, K // 2), dtype=torch.bfloat16, device=Wb.device)
+        mb = torch.empty((M, K // 8), dtype=torch.uint8, device=Wb.device)
+        for _ in range(3):
+            st.st24_prune_compress(Wb, vb, mb, stream=stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                st.st24_prune_compress(Wb, vb, mb, stream=stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / reps * 1e3
+        nbytes = M * K * 2 + M * K // 2 * 2 + M * K // 8
+        extra = {"shape": [M, K], "us_per_launch": us, "GB/s": nbytes / (us * 1e-6) / 1e9, "bytes": nbytes}
+        del Wb, vb, mb
     total_ms = ev[0][0].elapsed_time(ev[-1][2])
     prune_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
     spmm_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
     status = st.st24_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    return dict(total_ms=total_ms, prune_ms=prune_ms, spmm_ms=spmm_ms, clocks=clk.summary(),
+    return dict(total_ms=total_ms, prune_ms=prune_ms, spmm_ms=spmm_ms, clocks=clk.summary(), extra_prune=extra,
                 layers=layers, stream=stream, g_prune=g_prune, g_spmm=g_spmm)
 
 
@@ -341,6 +362,8 @@ def main():
     ap.add_argument("--impl", default="st24", choices=["st24", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "tcgen05", "mma_sp"],
+                    help="SpMM kernel family (auto = what st24_spmm picks)")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
 
@@ -348,7 +371,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
-    config = {"workload": w["desc"], "name": args.workload, "shapes": w["shapes"], "Ns": w["Ns"],
+    config = {"workload": w["desc"], "name": args.workload, "kernel": args.kernel, "shapes": w["shapes"], "Ns": w["Ns"],
               "layers": w["layers"], "ab": w["ab"], "out": w["c"],
               "l2": "inputs larger than L2: every step streams all weights (dense and compressed) from HBM"}
 
@@ -412,6 +435,8 @@ def main():
                         "spmm": {"launches_per_step": n_spmm(w), "us_per_launch": spmm_launch_ms * 1e3,
                                  "GB/s": spmm_gbs,
                                  "tflops_dense_equiv": flops / (r["spmm_ms"] / args.steps * 1e-3) / 1e12}}}
+    if r.get("extra_prune"):
+        line["kernels"]["prune_compress_bf16"] = r["extra_prune"]
     if rank == 0 and not args.no_e2e:
         e2e_ms, h2d, d2h = run_e2e(args, w, r["layers"], r["stream"])
         line["e2e"] = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -43,27 +43,28 @@ __device__ __forceinline__ uint32_t mag_key<kS8>(uint32_t raw) {
 }
 
 // Element i of a group outranks element j when its key is larger, or equal
-// with i < j.  The kept pair is the two elements outranked by fewer than two
-// others.  Returns the 4-bit keep mask (exactly two bits set).
-__device__ __forceinline__ uint32_t keep_mask(uint32_t k0, uint32_t k1, uint32_t k2, uint32_t k3) {
-  const uint32_t b0 = (k1 > k0) + (k2 > k0) + (k3 > k0);
-  const uint32_t b1 = (k0 >= k1) + (k2 > k1) + (k3 > k1);
-  const uint32_t b2 = (k0 >= k2) + (k1 >= k2) + (k3 > k2);
-  const uint32_t b3 = (k0 >= k3) + (k1 >= k3) + (k2 >= k3);
-  return (b0 < 2u) | ((b1 < 2u) << 1) | ((b2 < 2u) << 2) | ((b3 < 2u) << 3);
-}
-
-// One group: raw elements e[0..3] -> (v0, v1) with v0 at the lower index, and
-// the metadata nibble i0 | i1 << 2.
+// with i < j.  With c_ij = (k_i >= k_j) for i < j, element i is kept when it is
+// outranked by fewer than two others, i.e. when a majority of its three
+// comparisons go its way:
+//   keep0 = maj(c01, c02, c03)      keep1 = maj(!c01, c12, c13)
+//   keep2 = maj(!c02, !c12, c23)    keep3 = maj(!c03, !c13, !c23)
+// Exactly two of the four are kept (the relation is a strict total order).
+// Returns the nibble i0 | i1 << 2 of the kept pair and its two raw values.
 template <int DT>
 __device__ __forceinline__ uint32_t compress_group(const uint32_t (&e)[4], uint32_t& v0,
                                                    uint32_t& v1) {
-  const uint32_t keep =
-      keep_mask(mag_key<DT>(e[0]), mag_key<DT>(e[1]), mag_key<DT>(e[2]), mag_key<DT>(e[3]));
-  const uint32_t i0 = __ffs(keep) - 1;
-  const uint32_t i1 = 31 - __clz(keep);
-  v0 = i0 == 0 ? e[0] : (i0 == 1 ? e[1] : e[2]);
-  v1 = i1 == 3 ? e[3] : (i1 == 2 ? e[2] : e[1]);
+  const uint32_t k0 = mag_key<DT>(e[0]), k1 = mag_key<DT>(e[1]), k2 = mag_key<DT>(e[2]),
+                 k3 = mag_key<DT>(e[3]);
+  const bool c01 = k0 >= k1, c02 = k0 >= k2, c03 = k0 >= k3;
+  const bool c12 = k1 >= k2, c13 = k1 >= k3, c23 = k2 >= k3;
+  const bool keep0 = (c01 & c02) | (c01 & c03) | (c02 & c03);
+  const bool keep1 = (!c01 & c12) | (!c01 & c13) | (c12 & c13);
+  const bool keep2 = (!c02 & !c12) | (!c02 & c23) | (!c12 & c23);
+  const bool keep3 = (!c03 & !c13) | (!c03 & !c23) | (!c13 & !c23);
+  const uint32_t i0 = keep0 ? 0u : (keep1 ? 1u : 2u);
+  const uint32_t i1 = keep3 ? 3u : (keep2 ? 2u : 1u);
+  v0 = keep0 ? e[0] : (keep1 ? e[1] : e[2]);
+  v1 = keep3 ? e[3] : (keep2 ? e[2] : e[1]);
   return i0 | (i1 << 2);
 }
 
@@ -137,71 +138,85 @@ constexpr int kWarpSpan = 32 * kPiecesPerLane;  // pieces one warp handles per i
 
 // Fast path.  The matrix is a sequence of 16-byte pieces, `ppr` per row; warp
 // w handles pieces [w*128, w*128+128) of each grid-stride round, lane l the
-// pieces l, l+32, l+64 and l+96 of that span.
-template <int DT, int ES>
+// pieces l, l+32, l+64 and l+96 of that span.  A lane divides once per round
+// (Idx is 32-bit whenever the piece count allows) and carries (row, col)
+// forward for its other pieces.
+template <typename Idx>
+__device__ __forceinline__ void advance(Idx& row, Idx& col, Idx step, Idx ppr) {
+  col += step;
+  while (col >= ppr) {
+    col -= ppr;
+    ++row;
+  }
+}
+
+template <int DT, int ES, typename Idx>
 __global__ void __launch_bounds__(kThreads) prune_compress_vec(
-    const uint8_t* __restrict__ W, int64_t w_row_bytes, int64_t M, int64_t ppr,
+    const uint8_t* __restrict__ W, int64_t w_row_bytes, Idx total, Idx ppr,
     uint8_t* __restrict__ values, int64_t v_row_bytes, uint8_t* __restrict__ meta,
     int64_t m_row_bytes) {
-  const int64_t total = M * ppr;
   const int lane = threadIdx.x & 31;
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-  for (int64_t base = warp * kWarpSpan; base < total; base += nwarps * kWarpSpan) {
+  const Idx warp = (static_cast<Idx>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const Idx nwarps = (static_cast<Idx>(gridDim.x) * kThreads) >> 5;
+  for (Idx base = warp * kWarpSpan; base < total; base += nwarps * kWarpSpan) {
     uint4 in[kPiecesPerLane];
-    int64_t row[kPiecesPerLane], col[kPiecesPerLane];
+    Idx row[kPiecesPerLane], col[kPiecesPerLane];
+    Idx r = (base + lane) / ppr, c = base + lane - r * ppr;
 #pragma unroll
     for (int i = 0; i < kPiecesPerLane; ++i) {
-      const int64_t p = base + i * 32 + lane;
-      row[i] = p / ppr;
-      col[i] = p - row[i] * ppr;
-      if (p < total)
-        in[i] = __ldcs(reinterpret_cast<const uint4*>(W + row[i] * w_row_bytes + col[i] * 16));
+      row[i] = r;
+      col[i] = c;
+      if (base + i * 32 + lane < total)
+        in[i] = __ldcs(reinterpret_cast<const uint4*>(W + static_cast<int64_t>(r) * w_row_bytes +
+                                                      static_cast<int64_t>(c) * 16));
+      advance<Idx>(r, c, 32, ppr);
     }
 #pragma unroll
     for (int i = 0; i < kPiecesPerLane; ++i) {
       if (base + i * 32 + lane >= total) break;
       uint32_t mb;
       const uint2 v = compress_piece<DT, ES>(in[i], mb);
-      *reinterpret_cast<uint2*>(values + row[i] * v_row_bytes + col[i] * 8) = v;
+      const int64_t rr = row[i], cc = col[i];
+      *reinterpret_cast<uint2*>(values + rr * v_row_bytes + cc * 8) = v;
       if constexpr (ES == 2)
-        meta[row[i] * m_row_bytes + col[i]] = static_cast<uint8_t>(mb);
+        meta[rr * m_row_bytes + cc] = static_cast<uint8_t>(mb);
       else
-        *reinterpret_cast<uint16_t*>(meta + row[i] * m_row_bytes + col[i] * 2) =
-            static_cast<uint16_t>(mb);
+        *reinterpret_cast<uint16_t*>(meta + rr * m_row_bytes + cc * 2) = static_cast<uint16_t>(mb);
     }
   }
 }
 
-template <int ES>
+template <int ES, typename Idx>
 __global__ void __launch_bounds__(kThreads) decompress_vec(
     const uint8_t* __restrict__ values, int64_t v_row_bytes, const uint8_t* __restrict__ meta,
-    int64_t m_row_bytes, int64_t M, int64_t ppr, uint8_t* __restrict__ W, int64_t w_row_bytes) {
-  const int64_t total = M * ppr;
+    int64_t m_row_bytes, Idx total, Idx ppr, uint8_t* __restrict__ W, int64_t w_row_bytes) {
   const int lane = threadIdx.x & 31;
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-  for (int64_t base = warp * kWarpSpan; base < total; base += nwarps * kWarpSpan) {
+  const Idx warp = (static_cast<Idx>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const Idx nwarps = (static_cast<Idx>(gridDim.x) * kThreads) >> 5;
+  for (Idx base = warp * kWarpSpan; base < total; base += nwarps * kWarpSpan) {
     uint2 v[kPiecesPerLane];
     uint32_t mb[kPiecesPerLane];
-    int64_t row[kPiecesPerLane], col[kPiecesPerLane];
+    Idx row[kPiecesPerLane], col[kPiecesPerLane];
+    Idx r = (base + lane) / ppr, c = base + lane - r * ppr;
 #pragma unroll
     for (int i = 0; i < kPiecesPerLane; ++i) {
-      const int64_t p = base + i * 32 + lane;
-      row[i] = p / ppr;
-      col[i] = p - row[i] * ppr;
-      if (p < total) {
-        v[i] = __ldcs(reinterpret_cast<const uint2*>(values + row[i] * v_row_bytes + col[i] * 8));
+      row[i] = r;
+      col[i] = c;
+      if (base + i * 32 + lane < total) {
+        const int64_t rr = r, cc = c;
+        v[i] = __ldcs(reinterpret_cast<const uint2*>(values + rr * v_row_bytes + cc * 8));
         if constexpr (ES == 2)
-          mb[i] = __ldcs(meta + row[i] * m_row_bytes + col[i]);
+          mb[i] = __ldcs(meta + rr * m_row_bytes + cc);
         else
-          mb[i] = __ldcs(reinterpret_cast<const uint16_t*>(meta + row[i] * m_row_bytes + col[i] * 2));
+          mb[i] = __ldcs(reinterpret_cast<const uint16_t*>(meta + rr * m_row_bytes + cc * 2));
       }
+      advance<Idx>(r, c, 32, ppr);
     }
 #pragma unroll
     for (int i = 0; i < kPiecesPerLane; ++i) {
       if (base + i * 32 + lane >= total) break;
-      *reinterpret_cast<uint4*>(W + row[i] * w_row_bytes + col[i] * 16) = expand_piece<ES>(v[i], mb[i]);
+      const int64_t rr = row[i], cc = col[i];
+      *reinterpret_cast<uint4*>(W + rr * w_row_bytes + cc * 16) = expand_piece<ES>(v[i], mb[i]);
     }
   }
 }
@@ -272,26 +287,52 @@ __global__ void __launch_bounds__(kThreads) decompress_any(
 
 bool aligned(const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int grid_for(int64_t work_items, int items_per_block, int num_sms) {
+// Blocks that stay resident on one SM for kernel `k` (queried once per kernel).
+template <typename Kernel>
+int resident_blocks(Kernel k) {
+  static int blocks = 0;
+  if (blocks == 0) {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k, kThreads, 0) != cudaSuccess || b <= 0) b = 1;
+    blocks = b;
+  }
+  return blocks;
+}
+
+// A grid of at most one resident wave: every block stays on the GPU for the
+// whole launch and grid-strides over the work.
+template <typename Kernel>
+int grid_for(Kernel k, int64_t work_items, int items_per_block, int num_sms) {
   const int64_t want = (work_items + items_per_block - 1) / items_per_block;
-  const int64_t cap = static_cast<int64_t>(num_sms) * (2048 / kThreads);
+  const int64_t cap = static_cast<int64_t>(num_sms) * resident_blocks(k);
   return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
 }
+
+// 32-bit piece indices whenever the last grid-stride round cannot overflow them.
+inline bool fits_u32(int64_t total) { return total + (int64_t(1) << 26) < (int64_t(1) << 32); }
 
 template <int DT, int ES>
 void launch_pc(const void* W, int64_t M, int64_t K, int64_t ldw, void* values, void* meta,
                int num_sms, bool fast, cudaStream_t s) {
   if (fast) {
-    const int64_t ppr = K * ES / 16;
-    const int grid = grid_for(M * ppr, kThreads / 32 * kWarpSpan, num_sms);
-    prune_compress_vec<DT, ES><<<grid, kThreads, 0, s>>>(
-        static_cast<const uint8_t*>(W), ldw * ES, M, ppr, static_cast<uint8_t*>(values),
-        (K / 2) * ES, static_cast<uint8_t*>(meta), meta_row_bytes(K));
+    const int64_t ppr = K * ES / 16, total = M * ppr;
+    const auto* w = static_cast<const uint8_t*>(W);
+    auto* v = static_cast<uint8_t*>(values);
+    auto* e = static_cast<uint8_t*>(meta);
+    if (fits_u32(total)) {
+      auto k = prune_compress_vec<DT, ES, uint32_t>;
+      k<<<grid_for(k, total, kThreads / 32 * kWarpSpan, num_sms), kThreads, 0, s>>>(
+          w, ldw * ES, static_cast<uint32_t>(total), static_cast<uint32_t>(ppr), v, (K / 2) * ES, e,
+          meta_row_bytes(K));
+    } else {
+      auto k = prune_compress_vec<DT, ES, int64_t>;
+      k<<<grid_for(k, total, kThreads / 32 * kWarpSpan, num_sms), kThreads, 0, s>>>(
+          w, ldw * ES, total, ppr, v, (K / 2) * ES, e, meta_row_bytes(K));
+    }
   } else {
-    const int grid = grid_for(M * meta_row_bytes(K), kThreads, num_sms);
-    prune_compress_any<DT, ES><<<grid, kThreads, 0, s>>>(static_cast<const uint8_t*>(W), ldw, M, K,
-                                                         static_cast<uint8_t*>(values),
-                                                         static_cast<uint8_t*>(meta));
+    auto k = prune_compress_any<DT, ES>;
+    k<<<grid_for(k, M * meta_row_bytes(K), kThreads, num_sms), kThreads, 0, s>>>(
+        static_cast<const uint8_t*>(W), ldw, M, K, static_cast<uint8_t*>(values), static_cast<uint8_t*>(meta));
   }
 }
 
@@ -299,17 +340,24 @@ template <int ES>
 void launch_dc(const void* values, const void* meta, int64_t M, int64_t K, void* W, int64_t ldw,
                int num_sms, bool fast, cudaStream_t s) {
   if (fast) {
-    const int64_t ppr = K * ES / 16;
-    const int grid = grid_for(M * ppr, kThreads / 32 * kWarpSpan, num_sms);
-    decompress_vec<ES><<<grid, kThreads, 0, s>>>(static_cast<const uint8_t*>(values), (K / 2) * ES,
-                                                 static_cast<const uint8_t*>(meta),
-                                                 meta_row_bytes(K), M, ppr,
-                                                 static_cast<uint8_t*>(W), ldw * ES);
+    const int64_t ppr = K * ES / 16, total = M * ppr;
+    const auto* v = static_cast<const uint8_t*>(values);
+    const auto* e = static_cast<const uint8_t*>(meta);
+    auto* w = static_cast<uint8_t*>(W);
+    if (fits_u32(total)) {
+      auto k = decompress_vec<ES, uint32_t>;
+      k<<<grid_for(k, total, kThreads / 32 * kWarpSpan, num_sms), kThreads, 0, s>>>(
+          v, (K / 2) * ES, e, meta_row_bytes(K), static_cast<uint32_t>(total), static_cast<uint32_t>(ppr), w,
+          ldw * ES);
+    } else {
+      auto k = decompress_vec<ES, int64_t>;
+      k<<<grid_for(k, total, kThreads / 32 * kWarpSpan, num_sms), kThreads, 0, s>>>(
+          v, (K / 2) * ES, e, meta_row_bytes(K), total, ppr, w, ldw * ES);
+    }
   } else {
-    const int grid = grid_for(M * meta_row_bytes(K), kThreads, num_sms);
-    decompress_any<ES><<<grid, kThreads, 0, s>>>(static_cast<const uint8_t*>(values),
-                                                 static_cast<const uint8_t*>(meta), M, K,
-                                                 static_cast<uint8_t*>(W), ldw);
+    auto k = decompress_any<ES>;
+    k<<<grid_for(k, M * meta_row_bytes(K), kThreads, num_sms), kThreads, 0, s>>>(
+        static_cast<const uint8_t*>(values), static_cast<const uint8_t*>(meta), M, K, static_cast<uint8_t*>(W), ldw);
   }
 }
 

@@ -69,7 +69,8 @@ struct Config {
 
 struct Params : OutParams {
   int64_t K;
-  int64_t tiles_n, k_iters, total_iters;
+  int64_t tiles_n, k_iters, dp_tiles, sk_tiles;
+  int a_evict_first;      // A is read by one output tile only: stream it through L2
   float* partials;       // [2 * gridDim.x][PARTIAL_ELEMS]
   unsigned* counters;    // one per output tile
   unsigned* status;
@@ -135,8 +136,7 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x, cta = blockIdx.x;
-  const int64_t Ttot = p.total_iters, KI = p.k_iters;
-  const int64_t it_begin = iter_begin(cta, Ttot, G), it_end = iter_begin(cta + 1, Ttot, G);
+  const int64_t KI = p.k_iters;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmE);
       tma_prefetch_desc(&tmB);
-      const uint64_t stream_once = policy_evict_first();
+      const uint64_t stream_once = p.a_evict_first ? policy_evict_first() : policy_evict_last();
       const uint64_t reuse = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
@@ -161,10 +161,10 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
       bool issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = false;
       bool ok = true;
-      for (int64_t it = it_begin; it < it_end && ok;) {
-        const int64_t tile = it / KI;
-        const int64_t kb0 = it - tile * KI;
-        const int64_t kb1 = min(KI, kb0 + (it_end - it));
+      Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, cta);
+      Segment sg;
+      while (ok && sch.next(sg)) {
+        const int64_t tile = sg.tile, kb0 = sg.kb0, kb1 = sg.kb1;
         const int32_t mt = static_cast<int32_t>(tile / p.tiles_n);
         const int32_t nt = static_cast<int32_t>(tile - static_cast<int64_t>(mt) * p.tiles_n);
         for (int64_t kb = kb0; kb < kb1; ++kb) {
@@ -183,7 +183,6 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
           issued_parity[stage] = phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        it += kb1 - kb0;
       }
       // Never leave with copies in flight into this CTA's shared memory.
       for (int s = 0; s < STAGES; ++s)
@@ -197,10 +196,10 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
   const int gid = lane >> 2, tig = lane & 3;
   int stage = 0;
   uint32_t phase = 0;
-  for (int64_t it = it_begin; it < it_end;) {
-    const int64_t tile = it / KI;
-    const int64_t kb0 = it - tile * KI;
-    const int64_t kb1 = min(KI, kb0 + (it_end - it));
+  Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, cta);
+  Segment sg;
+  while (sch.next(sg)) {
+    const int64_t tile = sg.tile, kb0 = sg.kb0, kb1 = sg.kb1;
     const int64_t mt = tile / p.tiles_n, nt = tile - mt * p.tiles_n;
     const int64_t m_base = mt * Cfg::BM, n_base = nt * BN;
     Acc acc[2][WN][4];
@@ -263,9 +262,9 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
     bool write_out = whole;
     if (!whole) {
       // Partial tile: publish it, and let the last contributor finish the tile.
-      const int64_t c_lo = iter_owner(tile * KI, Ttot, G);
-      const int64_t c_hi = iter_owner(tile * KI + KI - 1, Ttot, G);
-      auto slot_of = [&](int64_t c) -> int64_t { return partial_slot(c, tile, Ttot, G, KI); };
+      const int64_t c_lo = sch.first_cta(tile);
+      const int64_t c_hi = sch.last_cta(tile);
+      auto slot_of = [&](int64_t c) -> int64_t { return sch.slot(c, tile); };
       float4* mine = reinterpret_cast<float4*>(p.partials + slot_of(cta) * Cfg::PARTIAL_ELEMS);
 #pragma unroll
       for (int i = 0; i < 2; ++i)
@@ -300,32 +299,37 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           Acc t[WN][4];
-          for (int64_t c = c_lo; c <= c_hi; ++c) {
-            Acc v[WN][4];
-            if (c == cta) {
+          constexpr int U = WN <= 4 ? 4 : 1;   // segments whose loads are issued together
+          for (int64_t cb = c_lo; cb <= c_hi; cb += U) {
+            float4 f[U][WN];
 #pragma unroll
-              for (int j = 0; j < WN; ++j)
+            for (int u = 0; u < U; ++u) {
+              if (cb + u <= c_hi && cb + u != cta) {
+                const float4* src = reinterpret_cast<const float4*>(p.partials + slot_of(cb + u) * Cfg::PARTIAL_ELEMS);
 #pragma unroll
-                for (int r = 0; r < 4; ++r) v[j][r] = acc[i][j][r];
-            } else {
-              const float4* src = reinterpret_cast<const float4*>(p.partials + slot_of(c) * Cfg::PARTIAL_ELEMS);
-              float4 f[WN];
-#pragma unroll
-              for (int j = 0; j < WN; ++j) f[j] = __ldcg(src + ((warp * 2 + i) * WN + j) * 32 + lane);
-#pragma unroll
-              for (int j = 0; j < WN; ++j) {
-                if constexpr (T::kInt) {
-                  v[j][0] = __float_as_int(f[j].x); v[j][1] = __float_as_int(f[j].y);
-                  v[j][2] = __float_as_int(f[j].z); v[j][3] = __float_as_int(f[j].w);
-                } else {
-                  v[j][0] = f[j].x; v[j][1] = f[j].y; v[j][2] = f[j].z; v[j][3] = f[j].w;
-                }
+                for (int j = 0; j < WN; ++j) f[u][j] = __ldcg(src + ((warp * 2 + i) * WN + j) * 32 + lane);
               }
             }
 #pragma unroll
-            for (int j = 0; j < WN; ++j)
+            for (int u = 0; u < U; ++u) {
+              const int64_t c = cb + u;
+              if (c > c_hi) break;
 #pragma unroll
-              for (int r = 0; r < 4; ++r) t[j][r] = (c == c_lo) ? v[j][r] : t[j][r] + v[j][r];
+              for (int j = 0; j < WN; ++j) {
+                Acc v[4];
+                if (c == cta) {
+#pragma unroll
+                  for (int r = 0; r < 4; ++r) v[r] = acc[i][j][r];
+                } else if constexpr (T::kInt) {
+                  v[0] = __float_as_int(f[u][j].x); v[1] = __float_as_int(f[u][j].y);
+                  v[2] = __float_as_int(f[u][j].z); v[3] = __float_as_int(f[u][j].w);
+                } else {
+                  v[0] = f[u][j].x; v[1] = f[u][j].y; v[2] = f[u][j].z; v[3] = f[u][j].w;
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) t[j][r] = (c == c_lo) ? v[r] : t[j][r] + v[r];
+              }
+            }
           }
 #pragma unroll
           for (int j = 0; j < WN; ++j)
@@ -346,7 +350,6 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
             if (m < p.M && n < p.N) store_out<Acc>(p, m, n, acc[i][j][r], row_factor(p, m));
           }
     }
-    it += kb1 - kb0;
   }
 }
 
@@ -369,7 +372,9 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
   p.M = a.M; p.N = a.N; p.K = a.K;
   p.tiles_n = plan.tiles_n;
   p.k_iters = plan.k_iters;
-  p.total_iters = plan.total_iters;
+  p.dp_tiles = plan.dp_tiles;
+  p.sk_tiles = plan.sk_tiles;
+  p.a_evict_first = plan.tiles_n == 1 ? 1 : 0;
   p.alpha = a.alpha; p.beta = a.beta;
   p.C = a.C; p.ldc = a.ldc; p.c_type = a.c;
   p.row_scale = a.row_scale;

@@ -84,7 +84,8 @@ struct TcConfig {
 
 struct TcParams : OutParams {
   int64_t K;
-  int64_t tiles_n, k_iters, total_iters;
+  int64_t tiles_n, k_iters, dp_tiles, sk_tiles;
+  int a_evict_first;      // A is read by one output tile only: stream it through L2
   float* partials;
   unsigned* counters;
   unsigned* status;
@@ -110,8 +111,7 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x, cta = blockIdx.x;
-  const int64_t Ttot = p.total_iters, KI = p.k_iters;
-  const int64_t it_begin = iter_begin(cta, Ttot, G), it_end = iter_begin(cta + 1, Ttot, G);
+  const int64_t KI = p.k_iters;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmE);
       tma_prefetch_desc(&tmB);
-      const uint64_t stream_once = policy_evict_first();
+      const uint64_t stream_once = p.a_evict_first ? policy_evict_first() : policy_evict_last();
       const uint64_t reuse = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
@@ -149,10 +149,10 @@ __global__ void __launch_bounds__(320, 1)
       bool issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = false;
       bool ok = true;
-      for (int64_t it = it_begin; it < it_end && ok;) {
-        const int64_t tile = it / KI;
-        const int64_t kb0 = it - tile * KI;
-        const int64_t kb1 = min(KI, kb0 + (it_end - it));
+      Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, cta);
+      Segment sg;
+      while (ok && sch.next(sg)) {
+        const int64_t tile = sg.tile, kb0 = sg.kb0, kb1 = sg.kb1;
         const int32_t mt = static_cast<int32_t>(tile / p.tiles_n);
         const int32_t nt = static_cast<int32_t>(tile - static_cast<int64_t>(mt) * p.tiles_n);
         for (int64_t kb = kb0; kb < kb1; ++kb) {
@@ -173,7 +173,6 @@ __global__ void __launch_bounds__(320, 1)
           issued_parity[stage] = phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        it += kb1 - kb0;
       }
       // Never leave with copies in flight into this CTA's shared memory.
       for (int s = 0; s < STAGES; ++s)
@@ -187,10 +186,10 @@ __global__ void __launch_bounds__(320, 1)
       int abuf = 0;
       uint32_t aphase = 0;
       bool ok = true;
-      for (int64_t it = it_begin; it < it_end && ok;) {
-        const int64_t tile = it / KI;
-        const int64_t kb0 = it - tile * KI;
-        const int64_t kb1 = min(KI, kb0 + (it_end - it));
+      Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, cta);
+      Segment sg;
+      while (ok && sch.next(sg)) {
+        const int64_t tile = sg.tile, kb0 = sg.kb0, kb1 = sg.kb1;
         if (!mbar_wait(smem_u32(&tempty_bar[abuf]), aphase ^ 1u, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(abuf * BN);
@@ -220,7 +219,6 @@ __global__ void __launch_bounds__(320, 1)
         if (!ok) break;
         tc_commit(smem_u32(&tfull_bar[abuf]));
         if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
-        it += kb1 - kb0;
       }
       // Every tcgen05 operation of this thread has completed before TMEM is freed.
       tc_commit(smem_u32(drain_bar));
@@ -234,10 +232,10 @@ __global__ void __launch_bounds__(320, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int64_t it = it_begin; it < it_end && ok;) {
-      const int64_t tile = it / KI;
-      const int64_t kb0 = it - tile * KI;
-      const int64_t kb1 = min(KI, kb0 + (it_end - it));
+    Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, cta);
+    Segment sg;
+    while (ok && sch.next(sg)) {
+      const int64_t tile = sg.tile, kb0 = sg.kb0, kb1 = sg.kb1;
       const int64_t rows_valid = p.M - (tile / p.tiles_n) * Cfg::BM;   // rows past M hold zero-filled metadata
       for (int64_t kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.status)) { ok = false; break; }
@@ -272,7 +270,6 @@ __global__ void __launch_bounds__(320, 1)
         if (lane == 0) mbar_arrive(smem_u32(&meta_bar[stage]));
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
-      it += kb1 - kb0;
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -280,10 +277,10 @@ __global__ void __launch_bounds__(320, 1)
     int abuf = 0;
     uint32_t aphase = 0;
     constexpr int CH = Cfg::CH;
-    for (int64_t it = it_begin; it < it_end;) {
-      const int64_t tile = it / KI;
-      const int64_t kb0 = it - tile * KI;
-      const int64_t kb1 = min(KI, kb0 + (it_end - it));
+    Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, cta);
+    Segment sg;
+    while (sch.next(sg)) {
+      const int64_t tile = sg.tile, kb0 = sg.kb0, kb1 = sg.kb1;
       const int64_t mt = tile / p.tiles_n, nt = tile - mt * p.tiles_n;
       const int64_t m = mt * Cfg::BM + 32 * q + lane;
       const int64_t n_base = nt * BN;
@@ -311,7 +308,7 @@ __global__ void __launch_bounds__(320, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[abuf]));
       } else {
-        float* mine = p.partials + partial_slot(cta, tile, Ttot, G, KI) * (Cfg::BM * BN);
+        float* mine = p.partials + sch.slot(cta, tile) * (Cfg::BM * BN);
 #pragma unroll 1
         for (int c = 0; c < BN; c += CH) {
           uint32_t r[CH];
@@ -325,8 +322,8 @@ __global__ void __launch_bounds__(320, 1)
         if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[abuf]));
         __threadfence();
         named_barrier_sync(1, 128);
-        const int64_t c_lo = iter_owner(tile * KI, Ttot, G);
-        const int64_t c_hi = iter_owner(tile * KI + KI - 1, Ttot, G);
+        const int64_t c_lo = sch.first_cta(tile);
+        const int64_t c_hi = sch.last_cta(tile);
         if (threadIdx.x == 64) {
           const unsigned nseg = static_cast<unsigned>(c_hi - c_lo + 1);
           const unsigned old = atomicAdd(p.counters + tile, 1u);
@@ -337,21 +334,33 @@ __global__ void __launch_bounds__(320, 1)
         }
         named_barrier_sync(1, 128);
         if (*s_last && row_ok) {
-          // Sum the partials in k order (segment c_lo first), CH columns at a
-          // time so each segment costs one batch of independent loads.
+          // Sum the partials in k order (segment c_lo first), RCH columns at a
+          // time; up to 4 segments' loads are issued together, so a tile split
+          // over s CTAs costs ceil(s / 4) memory latencies per column chunk.
+          constexpr int RCH = BN < 16 ? BN : 16;
 #pragma unroll 1
-          for (int c0 = 0; c0 < BN; c0 += CH) {
-            float t[CH];
-            for (int64_t c = c_lo; c <= c_hi; ++c) {
-              const float* src = p.partials + partial_slot(c, tile, Ttot, G, KI) * (Cfg::BM * BN) + 32 * q + lane;
-              float v[CH];
+          for (int c0 = 0; c0 < BN; c0 += RCH) {
+            float t[RCH];
+            for (int64_t cb = c_lo; cb <= c_hi; cb += 4) {
+              float v[4][RCH];
 #pragma unroll
-              for (int j = 0; j < CH; ++j) v[j] = __ldcg(src + (c0 + j) * Cfg::BM);
+              for (int u = 0; u < 4; ++u) {
+                if (cb + u <= c_hi) {
+                  const float* src = p.partials + sch.slot(cb + u, tile) * (Cfg::BM * BN) + 32 * q + lane;
 #pragma unroll
-              for (int j = 0; j < CH; ++j) t[j] = (c == c_lo) ? v[j] : t[j] + v[j];
+                  for (int j = 0; j < RCH; ++j) v[u][j] = __ldcg(src + (c0 + j) * Cfg::BM);
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                if (cb + u <= c_hi) {
+#pragma unroll
+                  for (int j = 0; j < RCH; ++j) t[j] = (cb + u == c_lo) ? v[u][j] : t[j] + v[u][j];
+                }
+              }
             }
 #pragma unroll
-            for (int j = 0; j < CH; ++j) {
+            for (int j = 0; j < RCH; ++j) {
               const int64_t n = n_base + c0 + j;
               if (n < p.N) store_out<float>(p, m, n, t[j], f);
             }
@@ -359,7 +368,6 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
-      it += kb1 - kb0;
     }
   }
 
@@ -389,7 +397,9 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
   p.row_scale = a.row_scale;
   p.tiles_n = plan.tiles_n;
   p.k_iters = plan.k_iters;
-  p.total_iters = plan.total_iters;
+  p.dp_tiles = plan.dp_tiles;
+  p.sk_tiles = plan.sk_tiles;
+  p.a_evict_first = plan.tiles_n == 1 ? 1 : 0;
   p.partials = static_cast<float*>(a.workspace);
   p.counters = plan.ws_bytes ? reinterpret_cast<unsigned*>(static_cast<uint8_t*>(a.workspace) +
                                                           2 * static_cast<size_t>(plan.grid) * plan.partial_bytes)

@@ -80,16 +80,28 @@ StreamKPlan make_stream_k_plan(int bm, int bn, int bk, int64_t M, int64_t N, int
   pl.tiles_m = (M + bm - 1) / bm;
   pl.tiles_n = (N + bn - 1) / bn;
   pl.k_iters = (K + bk - 1) / bk;
-  pl.total_iters = pl.tiles_m * pl.tiles_n * pl.k_iters;
-  const int64_t grid = pl.total_iters < num_sms ? pl.total_iters : num_sms;
+  const int64_t tiles = pl.tiles_m * pl.tiles_n;
+  const int64_t total_iters = tiles * pl.k_iters;
+  const int64_t grid = total_iters < num_sms ? total_iters : num_sms;
   pl.grid = static_cast<int>(grid > 0 ? grid : 1);
+  // Whole waves of tiles run data-parallel; the remainder plus one wave (so
+  // that each of its tiles is split over only one or two CTAs) runs stream-K.
+  if (tiles <= pl.grid) {
+    pl.sk_tiles = tiles;
+  } else {
+    const int64_t rem = tiles % pl.grid;
+    pl.sk_tiles = rem == 0 ? 0 : rem + pl.grid;
+  }
+  pl.dp_tiles = tiles - pl.sk_tiles;
   pl.partial_bytes = static_cast<size_t>(bm) * bn * 4;
-  // Is any tile split between CTAs?  (CTA c starts at iteration c*T/G.)
+  // Is any stream-K tile split between CTAs?  (CTA c starts at c*I/G.)
+  const int64_t sk_iters = pl.sk_tiles * pl.k_iters;
   bool split = false;
-  for (int64_t c = 1; c < pl.grid && !split; ++c)
-    if ((c * pl.total_iters / pl.grid) % pl.k_iters != 0) split = true;
-  const size_t tiles = static_cast<size_t>(pl.tiles_m * pl.tiles_n);
-  pl.ws_bytes = split ? 2 * static_cast<size_t>(pl.grid) * pl.partial_bytes + (tiles * 4 + 255) / 256 * 256 : 0;
+  for (int64_t c = 1; c < pl.grid && !split && sk_iters > 0; ++c)
+    if ((c * sk_iters / pl.grid) % pl.k_iters != 0) split = true;
+  pl.ws_bytes = split ? 2 * static_cast<size_t>(pl.grid) * pl.partial_bytes +
+                            (static_cast<size_t>(tiles) * 4 + 255) / 256 * 256
+                      : 0;
   return pl;
 }
 
@@ -111,6 +123,26 @@ StreamKPlan plan_for(int kernel, const SpmmArgs& a, int num_sms) {
 }
 
 }  // namespace
+
+st24_status st24::check_spmm_args(const SpmmArgs& a) {
+  if (!is_ab_type(a.ab) || a.M < 0 || a.N < 0 || a.K < 0 || a.K % 4 != 0)
+    return ST24_ERR_INVALID_ARG;
+  const bool float_out = a.c == kF32 || a.c == kBF16 || a.c == kF16;
+  if (!float_out && !(a.c == kS32 && a.ab == kS8)) return ST24_ERR_UNSUPPORTED;
+  if (a.c == kS32 && (a.alpha != 1.0f || a.beta != 0.0f || a.row_scale))
+    return ST24_ERR_UNSUPPORTED;
+  if (a.M == 0 || a.N == 0) return ST24_OK;
+  if (!a.C || a.ldc < a.M) return ST24_ERR_INVALID_ARG;
+  if (a.K > 0 && (!a.values || !a.meta || !a.B || a.ldb < a.K)) return ST24_ERR_INVALID_ARG;
+  if (a.K % 128 != 0) return ST24_ERR_UNSUPPORTED;
+  const int es = elem_size(a.ab);
+  if (a.K > 0 && (!aligned(a.values, 16) || !aligned(a.meta, 16) || !aligned(a.B, 16) ||
+                  (a.ldb * es) % 16 != 0))
+    return ST24_ERR_MISALIGNED;
+  if (!aligned(a.C, elem_size(a.c)) || (a.row_scale && !aligned(a.row_scale, 4)))
+    return ST24_ERR_MISALIGNED;
+  return ST24_OK;
+}
 
 extern "C" {
 
@@ -155,25 +187,6 @@ st24_status st24_decompress(st24_dtype type, const void* values, const void* met
   return launch_decompress(type, values, meta, M, K, W, ldw, static_cast<cudaStream_t>(stream));
 }
 
-static st24_status check_spmm(const SpmmArgs& a) {
-  if (!is_ab_type(a.ab) || a.M < 0 || a.N < 0 || a.K < 0 || a.K % 4 != 0)
-    return ST24_ERR_INVALID_ARG;
-  const bool float_out = a.c == kF32 || a.c == kBF16 || a.c == kF16;
-  if (!float_out && !(a.c == kS32 && a.ab == kS8)) return ST24_ERR_UNSUPPORTED;
-  if (a.c == kS32 && (a.alpha != 1.0f || a.beta != 0.0f || a.row_scale))
-    return ST24_ERR_UNSUPPORTED;
-  if (a.M == 0 || a.N == 0) return ST24_OK;
-  if (!a.C || a.ldc < a.M) return ST24_ERR_INVALID_ARG;
-  if (a.K > 0 && (!a.values || !a.meta || !a.B || a.ldb < a.K)) return ST24_ERR_INVALID_ARG;
-  if (a.K % 128 != 0) return ST24_ERR_UNSUPPORTED;
-  const int es = elem_size(a.ab);
-  if (a.K > 0 && (!aligned(a.values, 16) || !aligned(a.meta, 16) || !aligned(a.B, 16) ||
-                  (a.ldb * es) % 16 != 0))
-    return ST24_ERR_MISALIGNED;
-  if (!aligned(a.C, elem_size(a.c)) || (a.row_scale && !aligned(a.row_scale, 4)))
-    return ST24_ERR_MISALIGNED;
-  return ST24_OK;
-}
 
 size_t st24_spmm_workspace_bytes(st24_dtype ab_type, st24_dtype c_type, int64_t M, int64_t N,
                                  int64_t K) {
@@ -218,7 +231,7 @@ st24_status st24_spmm_ex(st24_kernel kernel, st24_dtype ab_type, st24_dtype c_ty
   a.row_scale = row_scale;
   a.workspace = workspace;
   a.ws_bytes = ws_bytes;
-  st24_status st = check_spmm(a);
+  st24_status st = check_spmm_args(a);
   if (st != ST24_OK || M == 0 || N == 0) return st;
   const int k = resolve_kernel(kernel, ab_type);
   if (k == ST24_KERNEL_TCGEN05 && ab_type == ST24_S8) return ST24_ERR_UNSUPPORTED;

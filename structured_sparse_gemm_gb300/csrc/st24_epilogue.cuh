@@ -10,6 +10,7 @@
 #include <type_traits>
 
 #include "st24_device.cuh"
+#include "st24_schedule.cuh"
 
 namespace st24 {
 
@@ -55,20 +56,5 @@ __device__ __forceinline__ void store_out(const OutParams& p, int64_t m, int64_t
 
 // C = beta * C over the whole M x N output (the product is empty when K == 0).
 __global__ void scale_c_kernel(OutParams p);
-
-// ---- stream-K schedule (shared by the persistent kernels) -------------------
-// Iterations (tile, k-block) are numbered tile * k_iters + kb; CTA c of G runs
-// [c*T/G, (c+1)*T/G).
-__device__ __forceinline__ int64_t iter_begin(int64_t c, int64_t T, int64_t G) { return c * T / G; }
-// The CTA whose run contains iteration u.
-__device__ __forceinline__ int64_t iter_owner(int64_t u, int64_t T, int64_t G) {
-  return ((u + 1) * G - 1) / T;
-}
-// Workspace slot of CTA c's partial of `tile`: 2c for the first tile of its run,
-// 2c + 1 for the last (a run has at most these two partial tiles).
-__device__ __forceinline__ int64_t partial_slot(int64_t c, int64_t tile, int64_t T, int64_t G,
-                                                int64_t k_iters) {
-  return 2 * c + ((iter_begin(c, T, G) / k_iters) == tile ? 0 : 1);
-}
 
 }  // namespace st24

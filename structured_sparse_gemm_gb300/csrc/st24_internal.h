@@ -60,13 +60,14 @@ struct SpmmArgs {
   size_t ws_bytes;
 };
 
-// A split of the output into tiles and of each tile's K loop into iterations,
-// shared out over a persistent grid (stream-K: every CTA gets a contiguous
-// run of the flattened (tile, k-iteration) space).
+// A split of the output into BM x BN tiles and of each tile's K loop into
+// k-blocks, shared out over a persistent grid: dp_tiles whole tiles in
+// data-parallel waves, then sk_tiles tiles whose (tile, k-block) iterations are
+// split evenly over the grid (stream-K).
 struct StreamKPlan {
   int bm, bn, bk;          // tile shape; bk in logical K
   int64_t tiles_m, tiles_n, k_iters;
-  int64_t total_iters;
+  int64_t dp_tiles, sk_tiles;
   int grid;                // CTAs
   size_t partial_bytes;    // bytes of one fp32 partial tile
   size_t ws_bytes;         // workspace bytes (0 if no tile is split)
@@ -74,6 +75,9 @@ struct StreamKPlan {
 
 // A stream-K plan over a persistent grid of at most num_sms CTAs.
 StreamKPlan make_stream_k_plan(int bm, int bn, int bk, int64_t M, int64_t N, int64_t K, int num_sms);
+
+// Host-side argument checks of st24_spmm (no CUDA call is made).
+st24_status check_spmm_args(const SpmmArgs& a);
 
 // The mma.sp (warp-level sparse MMA) path: every element type.
 StreamKPlan plan_spmm_mmasp(const SpmmArgs& a, int num_sms);
