@@ -187,6 +187,38 @@ ST24_API st24_status st24_spmm_ex(st24_kernel kernel, st24_dtype ab_type, st24_d
                                   void* stream);
 
 /*
+ * st24_spmm for callers that cannot allocate device memory.  No counterpart
+ * in the source pages: it is a deployment variant of st24_spmm.
+ *
+ * Some callers cannot call cudaMalloc or take memory from an allocator: a
+ * plugin inside a serving runtime whose device memory is owned entirely by
+ * the runtime's pool, code that runs while a stream is being captured in the
+ * global capture mode (where cudaMalloc is not allowed), or a latency-critical
+ * path that must not take the allocator's lock or synchronise the device.
+ * This call takes the same arguments as st24_spmm without the workspace and
+ * keeps the split-K / stream-K partial tiles and tile counters in a
+ * fixed-size array in device global memory owned by the library: 16 MiB on
+ * every GPU that loads the library, held until the process exits.  It calls
+ * no cudaMalloc, cudaFree or allocating library routine.
+ *   - A product whose schedule needs more scratch than 16 MiB (for example
+ *     N > 64 with a stream-K tail on a large M) returns ST24_ERR_WORKSPACE and
+ *     launches nothing; every product with N <= 64 fits.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's contents; each call clears the tile counters (a cudaMemsetAsync
+ *     on `stream`) before its kernel.  Calls whose work overlaps on the GPU
+ *     (on different streams, or from different host threads) race on the
+ *     array and give wrong results: serialise them.
+ * Results are identical to st24_spmm with a workspace of its own.
+ */
+ST24_API st24_status st24_spmm_noalloc(st24_dtype ab_type, st24_dtype c_type, int64_t M, int64_t N,
+                                       int64_t K, float alpha, const void* A_values, const void* A_meta,
+                                       const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
+                                       const float* row_scale, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the status word the kernels
  * of the current device write when a bounded wait runs out
  * (ST24_ERR_TIMEOUT), or returns ST24_ERR_CUDA if the stream reports an

@@ -21,7 +21,7 @@ from . import _build_lib
 __all__ = [
     "St24Error", "load", "st24_version", "st24_status_string", "st24_values_bytes",
     "st24_meta_bytes", "st24_prune_compress", "st24_decompress", "st24_spmm_workspace_bytes",
-    "st24_spmm", "st24_spmm_ex", "st24_device_status", "dtype_code", "compress", "spmm", "Workspace",
+    "st24_spmm", "st24_spmm_ex", "st24_spmm_noalloc", "st24_device_status", "dtype_code", "compress", "spmm", "Workspace",
 ]
 
 F16, BF16, E4M3, S8, F32, S32 = 0, 1, 2, 3, 4, 5
@@ -69,6 +69,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.st24_spmm.restype = i
     lib.st24_spmm_ex.argtypes = [i, i, i, i64, i64, i64, f, p, p, p, i64, f, p, i64, p, p, sz, p]
     lib.st24_spmm_ex.restype = i
+    lib.st24_spmm_noalloc.argtypes = [i, i, i64, i64, i64, f, p, p, p, i64, f, p, i64, p, p]
+    lib.st24_spmm_noalloc.restype = i
     lib.st24_device_status.argtypes = [p]
     lib.st24_device_status.restype = i
     _lib = lib
@@ -164,6 +166,20 @@ def st24_spmm(values: torch.Tensor, meta: torch.Tensor, X: torch.Tensor, Y: torc
         _check(load().st24_spmm(*args), "st24_spmm")
     else:
         _check(load().st24_spmm_ex(k, *args), "st24_spmm_ex")
+
+
+def st24_spmm_noalloc(values: torch.Tensor, meta: torch.Tensor, X: torch.Tensor, Y: torch.Tensor, *,
+                      K: int | None = None, alpha: float = 1.0, beta: float = 0.0,
+                      row_scale: torch.Tensor | None = None, M: int | None = None, stream=None) -> None:
+    """st24_spmm with the library's own fixed-size scratch (for callers that cannot allocate)."""
+    N, Kx = X.shape
+    K = Kx if K is None else K
+    M = Y.shape[1] if M is None else M
+    if X.stride(1) != 1 or Y.stride(1) != 1:
+        raise ValueError("X and Y must have unit stride along their last dimension")
+    _check(load().st24_spmm_noalloc(dtype_code(X.dtype), dtype_code(Y.dtype), M, N, K, float(alpha), _ptr(values),
+                                    _ptr(meta), _ptr(X), X.stride(0), float(beta), _ptr(Y), Y.stride(0),
+                                    _ptr(row_scale), _stream(stream)), "st24_spmm_noalloc")
 
 
 def st24_device_status(stream=None) -> int:
