@@ -69,8 +69,9 @@ struct Config {
 
 struct Params : OutParams {
   int64_t K;
-  int64_t tiles_n, k_iters, dp_tiles, sk_tiles;
+  int64_t tiles_m, tiles_n, group_m, k_iters, dp_tiles, sk_tiles;
   int a_evict_first;      // A is read by one output tile only: stream it through L2
+  int cluster;            // > 1: the CTAs of each split tile form a cluster and reduce in shared memory
   float* partials;       // [2 * gridDim.x][PARTIAL_ELEMS]
   unsigned* counters;    // one per output tile
   unsigned* status;
@@ -146,6 +147,10 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
     fence_barrier_init();
   }
   __syncthreads();
+  // Everything above overlaps the previous kernel in the stream; inputs are
+  // read only after it has completed.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
 
   if (warp == Cfg::CONSUMERS) {
     // ------------------------------------------------------------ producer
@@ -165,8 +170,9 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
       Segment sg;
       while (ok && sch.next(sg)) {
         const int64_t tile = sg.tile, kb0 = sg.kb0, kb1 = sg.kb1;
-        const int32_t mt = static_cast<int32_t>(tile / p.tiles_n);
-        const int32_t nt = static_cast<int32_t>(tile - static_cast<int64_t>(mt) * p.tiles_n);
+        int64_t mt64, nt64;
+        tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mt64, nt64);
+        const int32_t mt = static_cast<int32_t>(mt64), nt = static_cast<int32_t>(nt64);
         for (int64_t kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full_bar[stage]);
@@ -188,11 +194,19 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
       for (int s = 0; s < STAGES; ++s)
         if (issued[s]) mbar_wait(smem_u32(&full_bar[s]), issued_parity[s], p.status);
     }
+    __syncwarp();
+    if (p.cluster > 1) {
+      // The producer warp takes part in the two cluster barriers of the
+      // in-cluster reduction (see the consumers).
+      cluster_sync();
+      cluster_sync();
+    }
     return;
   }
 
   // -------------------------------------------------------------- consumers
   const int wm = warp % Cfg::WARPS_M, wn = warp / Cfg::WARPS_M;
+  int cluster_done = 0;   // cluster barriers passed (cluster mode: exactly two per CTA)
   const int gid = lane >> 2, tig = lane & 3;
   int stage = 0;
   uint32_t phase = 0;
@@ -200,7 +214,8 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
   Segment sg;
   while (sch.next(sg)) {
     const int64_t tile = sg.tile, kb0 = sg.kb0, kb1 = sg.kb1;
-    const int64_t mt = tile / p.tiles_n, nt = tile - mt * p.tiles_n;
+    int64_t mt, nt;
+    tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
     const int64_t m_base = mt * Cfg::BM, n_base = nt * BN;
     Acc acc[2][WN][4];
 #pragma unroll
@@ -260,7 +275,64 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
     // ---- epilogue ----
     const bool whole = (kb0 == 0 && kb1 == KI);
     bool write_out = whole;
-    if (!whole) {
+    bool mine[2][WN];          // fragments this CTA writes out
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int j = 0; j < WN; ++j) mine[i][j] = true;
+    if (!whole && p.cluster > 1) {
+      // Split-K inside the cluster: CTA rank r of the cluster holds the r-th
+      // k-range of this tile.  Every CTA parks its fragments in its own shared
+      // memory (the stage ring, idle now); after a cluster barrier each CTA
+      // sums a 1/cluster share of the fragments over the ranks in order and
+      // writes it out; a second barrier keeps the memory alive until all
+      // peers have read it.
+      consumer_sync(Cfg::CONSUMERS * 32);
+      float4* part = reinterpret_cast<float4*>(smem);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < WN; ++j) {
+          const int f = (warp * 2 + i) * WN + j;
+          if constexpr (T::kInt)
+            part[f * 32 + lane] = make_float4(__int_as_float(acc[i][j][0]), __int_as_float(acc[i][j][1]),
+                                              __int_as_float(acc[i][j][2]), __int_as_float(acc[i][j][3]));
+          else
+            part[f * 32 + lane] = make_float4(acc[i][j][0], acc[i][j][1], acc[i][j][2], acc[i][j][3]);
+        }
+      cluster_sync();
+      cluster_done = 1;
+      const int rank = static_cast<int>(cluster_ctarank());
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < WN; ++j) {
+          const int f = (warp * 2 + i) * WN + j;
+          mine[i][j] = (f % p.cluster) == rank;
+          if (!mine[i][j]) continue;
+          float4 v[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (q < p.cluster) v[q] = ld_shared_cluster_f4(part + f * 32 + lane, static_cast<uint32_t>(q));
+          Acc t[4];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            if (q >= p.cluster) break;
+            Acc u[4];
+            if constexpr (T::kInt) {
+              u[0] = __float_as_int(v[q].x); u[1] = __float_as_int(v[q].y);
+              u[2] = __float_as_int(v[q].z); u[3] = __float_as_int(v[q].w);
+            } else {
+              u[0] = v[q].x; u[1] = v[q].y; u[2] = v[q].z; u[3] = v[q].w;
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) t[r] = (q == 0) ? u[r] : t[r] + u[r];
+          }
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[i][j][r] = t[r];
+        }
+      write_out = true;
+    } else if (!whole) {
       // Partial tile: publish it, and let the last contributor finish the tile.
       const int64_t c_lo = sch.first_cta(tile);
       const int64_t c_hi = sch.last_cta(tile);
@@ -339,18 +411,41 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
       }
     }
     if (write_out) {
+      // All of this thread's C inputs are read before any output is written.
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < 2; ++i) {
+        float bc[WN][4];
 #pragma unroll
         for (int j = 0; j < WN; ++j)
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int64_t m = m_base + wm * 32 + i * 16 + gid + 8 * (r >> 1);
             const int64_t n = n_base + wn * WN * 8 + j * 8 + 2 * tig + (r & 1);
-            if (m < p.M && n < p.N) store_out<Acc>(p, m, n, acc[i][j][r], row_factor(p, m));
+            bc[j][r] = (mine[i][j] && m < p.M && n < p.N) ? load_beta_c(p, m, n) : 0.0f;
           }
+#pragma unroll
+        for (int j = 0; j < WN; ++j)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int64_t m = m_base + wm * 32 + i * 16 + gid + 8 * (r >> 1);
+            const int64_t n = n_base + wn * WN * 8 + j * 8 + 2 * tig + (r & 1);
+            if (mine[i][j] && m < p.M && n < p.N)
+              store_out<Acc>(p, m, n, acc[i][j][r], row_factor(p, m), bc[j][r]);
+          }
+      }
+    }
+    if (cluster_done == 1) {
+      cluster_sync();   // peers have finished reading this CTA's shared memory
+      cluster_done = 2;
     }
   }
+  // A wait that ran out of time skipped the reduction: still meet the peers
+  // at both cluster barriers.
+  if (p.cluster > 1)
+    while (cluster_done < 2) {
+      cluster_sync();
+      ++cluster_done;
+    }
 }
 
 template <int DT, int BN, int WARPS_N, int STAGES>
@@ -370,11 +465,14 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
     return ST24_ERR_CUDA;
   Params p{};
   p.M = a.M; p.N = a.N; p.K = a.K;
+  p.tiles_m = plan.tiles_m;
   p.tiles_n = plan.tiles_n;
+  p.group_m = plan.group_m;
   p.k_iters = plan.k_iters;
   p.dp_tiles = plan.dp_tiles;
   p.sk_tiles = plan.sk_tiles;
   p.a_evict_first = plan.tiles_n == 1 ? 1 : 0;
+  p.cluster = plan.cluster;
   p.alpha = a.alpha; p.beta = a.beta;
   p.C = a.C; p.ldc = a.ldc; p.c_type = a.c;
   p.row_scale = a.row_scale;
@@ -392,8 +490,29 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
       return ST24_ERR_CUDA;
     attr_set[dev.device % 64] = true;
   }
-  kern<<<plan.grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmE, tmB, p);
-  return cudaGetLastError() == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;
+  // Launched as a programmatic dependent of the previous kernel in the stream
+  // (its prologue overlaps that kernel's tail), and in clusters of
+  // plan.cluster CTAs when split tiles are reduced inside the cluster.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  unsigned n = 0;
+  attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (plan.cluster > 1) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = static_cast<unsigned>(plan.cluster);
+    attrs[n].val.clusterDim.y = 1;
+    attrs[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmE, tmB, p) == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;
 }
 
 template <int DT>

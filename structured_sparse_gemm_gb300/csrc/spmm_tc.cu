@@ -14,7 +14,9 @@ static int pick_bn_tc(int64_t N) {
 }
 
 StreamKPlan plan_spmm_tc(const SpmmArgs& a, int num_sms) {
-  return make_stream_k_plan(128, pick_bn_tc(a.N), elem_size(a.ab) == 2 ? 128 : 256, a.M, a.N, a.K, num_sms);
+  return make_stream_k_plan(128, pick_bn_tc(a.N), elem_size(a.ab) == 2 ? 128 : 256, a.M, a.N, a.K, num_sms,
+                            a.K * (elem_size(a.ab) / 2.0 + 0.125), static_cast<double>(a.K) * elem_size(a.ab),
+                            false);
 }
 
 st24_status launch_spmm_tc(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev,

@@ -84,7 +84,7 @@ struct TcConfig {
 
 struct TcParams : OutParams {
   int64_t K;
-  int64_t tiles_n, k_iters, dp_tiles, sk_tiles;
+  int64_t tiles_m, tiles_n, group_m, k_iters, dp_tiles, sk_tiles;
   int a_evict_first;      // A is read by one output tile only: stream it through L2
   float* partials;
   unsigned* counters;
@@ -134,6 +134,10 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The prologue above overlaps the previous kernel in the stream; inputs are
+  // read only after it has completed.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -153,8 +157,9 @@ __global__ void __launch_bounds__(320, 1)
       Segment sg;
       while (ok && sch.next(sg)) {
         const int64_t tile = sg.tile, kb0 = sg.kb0, kb1 = sg.kb1;
-        const int32_t mt = static_cast<int32_t>(tile / p.tiles_n);
-        const int32_t nt = static_cast<int32_t>(tile - static_cast<int64_t>(mt) * p.tiles_n);
+        int64_t mt64, nt64;
+        tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mt64, nt64);
+        const int32_t mt = static_cast<int32_t>(mt64), nt = static_cast<int32_t>(nt64);
         for (int64_t kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full_bar[stage]);
@@ -236,7 +241,9 @@ __global__ void __launch_bounds__(320, 1)
     Segment sg;
     while (ok && sch.next(sg)) {
       const int64_t tile = sg.tile, kb0 = sg.kb0, kb1 = sg.kb1;
-      const int64_t rows_valid = p.M - (tile / p.tiles_n) * Cfg::BM;   // rows past M hold zero-filled metadata
+      int64_t mt, nt;
+      tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
+      const int64_t rows_valid = p.M - mt * Cfg::BM;   // rows past M hold zero-filled metadata
       for (int64_t kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.status)) { ok = false; break; }
         const uint8_t* se = smem + stage * Cfg::STAGE_BYTES + Cfg::A_BYTES + Cfg::B_BYTES;
@@ -281,7 +288,8 @@ __global__ void __launch_bounds__(320, 1)
     Segment sg;
     while (sch.next(sg)) {
       const int64_t tile = sg.tile, kb0 = sg.kb0, kb1 = sg.kb1;
-      const int64_t mt = tile / p.tiles_n, nt = tile - mt * p.tiles_n;
+      int64_t mt, nt;
+      tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
       const int64_t m = mt * Cfg::BM + 32 * q + lane;
       const int64_t n_base = nt * BN;
       if (!mbar_wait(smem_u32(&tfull_bar[abuf]), aphase, p.status)) break;
@@ -297,10 +305,13 @@ __global__ void __launch_bounds__(320, 1)
           if constexpr (CH == 32) tmem_ld_x32(tacc + c, r); else tmem_ld_x16(tacc + c, r);
           tmem_ld_wait();
           if (row_ok) {
+            float bc[CH];
+#pragma unroll
+            for (int j = 0; j < CH; ++j) bc[j] = (n_base + c + j < p.N) ? load_beta_c(p, m, n_base + c + j) : 0.0f;
 #pragma unroll
             for (int j = 0; j < CH; ++j) {
               const int64_t n = n_base + c + j;
-              if (n < p.N) store_out<float>(p, m, n, __uint_as_float(r[j]), f);
+              if (n < p.N) store_out<float>(p, m, n, __uint_as_float(r[j]), f, bc[j]);
             }
           }
         }
@@ -359,10 +370,13 @@ __global__ void __launch_bounds__(320, 1)
                 }
               }
             }
+            float bc[RCH];
+#pragma unroll
+            for (int j = 0; j < RCH; ++j) bc[j] = (n_base + c0 + j < p.N) ? load_beta_c(p, m, n_base + c0 + j) : 0.0f;
 #pragma unroll
             for (int j = 0; j < RCH; ++j) {
               const int64_t n = n_base + c0 + j;
-              if (n < p.N) store_out<float>(p, m, n, t[j], f);
+              if (n < p.N) store_out<float>(p, m, n, t[j], f, bc[j]);
             }
           }
         }
@@ -395,7 +409,9 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
   p.alpha = a.alpha; p.beta = a.beta;
   p.C = a.C; p.ldc = a.ldc; p.c_type = a.c;
   p.row_scale = a.row_scale;
+  p.tiles_m = plan.tiles_m;
   p.tiles_n = plan.tiles_n;
+  p.group_m = plan.group_m;
   p.k_iters = plan.k_iters;
   p.dp_tiles = plan.dp_tiles;
   p.sk_tiles = plan.sk_tiles;
@@ -412,8 +428,18 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
       return ST24_ERR_CUDA;
     attr_set[dev.device % 64] = true;
   }
-  kern<<<plan.grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmE, tmB, p);
-  return cudaGetLastError() == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;
+  // Launched as a programmatic dependent of the previous kernel in the stream.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmE, tmB, p) == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;
 }
 
 template <int DT>

@@ -72,7 +72,8 @@ bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, const void
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-StreamKPlan make_stream_k_plan(int bm, int bn, int bk, int64_t M, int64_t N, int64_t K, int num_sms) {
+StreamKPlan make_stream_k_plan(int bm, int bn, int bk, int64_t M, int64_t N, int64_t K, int num_sms,
+                               double a_row_bytes, double b_col_bytes, bool allow_cluster) {
   StreamKPlan pl{};
   pl.bm = bm;
   pl.bn = bn;
@@ -82,7 +83,12 @@ StreamKPlan make_stream_k_plan(int bm, int bn, int bk, int64_t M, int64_t N, int
   pl.k_iters = (K + bk - 1) / bk;
   const int64_t tiles = pl.tiles_m * pl.tiles_n;
   const int64_t total_iters = tiles * pl.k_iters;
-  const int64_t grid = total_iters < num_sms ? total_iters : num_sms;
+  // Fewer tiles than SMs: split every tile over the same number of CTAs
+  // (tiles * floor(SMs / tiles)) so each CTA streams an equal, whole-k-block
+  // share and every split tile has the same few contributors.
+  int64_t grid = num_sms;
+  if (tiles > 0 && tiles < num_sms) grid = tiles * (num_sms / tiles);
+  if (grid > total_iters) grid = total_iters;
   pl.grid = static_cast<int>(grid > 0 ? grid : 1);
   // Whole waves of tiles run data-parallel; the remainder plus one wave (so
   // that each of its tiles is split over only one or two CTAs) runs stream-K.
@@ -93,7 +99,31 @@ StreamKPlan make_stream_k_plan(int bm, int bn, int bk, int64_t M, int64_t N, int
     pl.sk_tiles = rem == 0 ? 0 : rem + pl.grid;
   }
   pl.dp_tiles = tiles - pl.sk_tiles;
+  // Raster.  Consecutive tiles run at the same time; keep one operand's panel
+  // in L2 and stream the other once.  If all of B fits in the budget, go
+  // row by row (m-tile outer): B stays resident, A is read once.  Otherwise
+  // group as many m-tiles as fit (their A panel stays resident) and sweep the
+  // n-tiles inside each group, so B is read once per group.
+  const double kResident = 56.0 * (1 << 20);
+  if (b_col_bytes * static_cast<double>(N) <= kResident) {
+    pl.group_m = 1;
+  } else {
+    const double per_mtile = a_row_bytes * bm;
+    int64_t g = static_cast<int64_t>(kResident / (per_mtile > 1.0 ? per_mtile : 1.0));
+    pl.group_m = g < 1 ? 1 : (g > pl.tiles_m ? pl.tiles_m : g);
+  }
   pl.partial_bytes = static_cast<size_t>(bm) * bn * 4;
+  // Every tile split over the same s = grid / tiles CTAs (2 <= s <= 8, whole
+  // k-blocks each): those CTAs can form one cluster and sum in shared memory.
+  pl.cluster = 1;
+  if (allow_cluster && pl.dp_tiles == 0 && tiles > 0 && pl.grid % tiles == 0) {
+    const int64_t sp = pl.grid / tiles;
+    if (sp >= 2 && sp <= 8 && pl.k_iters >= sp) pl.cluster = static_cast<int>(sp);
+  }
+  if (pl.cluster > 1) {
+    pl.ws_bytes = 0;
+    return pl;
+  }
   // Is any stream-K tile split between CTAs?  (CTA c starts at c*I/G.)
   const int64_t sk_iters = pl.sk_tiles * pl.k_iters;
   bool split = false;
@@ -113,9 +143,16 @@ namespace {
 
 // The kernel family a call runs on: tcgen05 for the 16-bit and fp8 inputs,
 // the warp-level sparse MMA for int8 (there is no int8 tcgen05 kind on sm_103a).
-int resolve_kernel(int requested, int ab) {
-  if (requested == ST24_KERNEL_AUTO) return ab == kS8 ? ST24_KERNEL_MMA_SP : ST24_KERNEL_TCGEN05;
-  return requested;
+// Products whose arithmetic intensity is low enough to be bound by streaming
+// the compressed A from HBM (2N flops per logical weight over s/2 + 1/8 bytes,
+// at most 64 flop/B: N <= 32 for 16-bit inputs, N <= 16 for fp8) run on the
+// warp-level kernel, which has less fixed latency per launch (measured);
+// int8 always does (no int8 tcgen05 kind on sm_103a); the rest run on tcgen05.
+int resolve_kernel(int requested, int ab, int64_t N) {
+  if (requested != ST24_KERNEL_AUTO) return requested;
+  if (ab == kS8) return ST24_KERNEL_MMA_SP;
+  const double intensity = 2.0 * static_cast<double>(N) / (elem_size(ab) / 2.0 + 0.125);
+  return intensity <= 64.0 ? ST24_KERNEL_MMA_SP : ST24_KERNEL_TCGEN05;
 }
 
 StreamKPlan plan_for(int kernel, const SpmmArgs& a, int num_sms) {
@@ -123,6 +160,10 @@ StreamKPlan plan_for(int kernel, const SpmmArgs& a, int num_sms) {
 }
 
 }  // namespace
+
+StreamKPlan st24::plan_auto(const SpmmArgs& a, int num_sms) {
+  return plan_for(resolve_kernel(ST24_KERNEL_AUTO, a.ab, a.N), a, num_sms);
+}
 
 st24_status st24::check_spmm_args(const SpmmArgs& a) {
   if (!is_ab_type(a.ab) || a.M < 0 || a.N < 0 || a.K < 0 || a.K % 4 != 0)
@@ -233,7 +274,7 @@ st24_status st24_spmm_ex(st24_kernel kernel, st24_dtype ab_type, st24_dtype c_ty
   a.ws_bytes = ws_bytes;
   st24_status st = check_spmm_args(a);
   if (st != ST24_OK || M == 0 || N == 0) return st;
-  const int k = resolve_kernel(kernel, ab_type);
+  const int k = resolve_kernel(kernel, ab_type, N);
   if (k == ST24_KERNEL_TCGEN05 && ab_type == ST24_S8) return ST24_ERR_UNSUPPORTED;
   const DeviceInfo* dev = current_device_info();
   if (!dev) return ST24_ERR_CUDA;

@@ -36,8 +36,17 @@ __device__ __forceinline__ float row_factor(const OutParams& p, int64_t m) {
   return p.row_scale ? __fmul_rn(p.alpha, p.row_scale[m]) : p.alpha;
 }
 
+// beta * C(m, n) as read before any output of the chunk is written (0 when
+// beta == 0: C is not read).  Load a chunk's inputs first, then store the
+// chunk: C is read and written through the same pointer, so a load placed
+// after a store to C has to wait for it.
+__device__ __forceinline__ float load_beta_c(const OutParams& p, int64_t m, int64_t n) {
+  return p.beta != 0.0f ? __fmul_rn(p.beta, load_c(p, n * p.ldc + m)) : 0.0f;
+}
+
 template <typename Acc>
-__device__ __forceinline__ void store_out(const OutParams& p, int64_t m, int64_t n, Acc acc, float factor) {
+__device__ __forceinline__ void store_out(const OutParams& p, int64_t m, int64_t n, Acc acc, float factor,
+                                          float beta_c) {
   const int64_t idx = n * p.ldc + m;
   if constexpr (std::is_same<Acc, int>::value) {
     if (p.c_type == kS32) {
@@ -46,7 +55,7 @@ __device__ __forceinline__ void store_out(const OutParams& p, int64_t m, int64_t
     }
   }
   float r = __fmul_rn(static_cast<float>(acc), factor);
-  if (p.beta != 0.0f) r = __fadd_rn(r, __fmul_rn(p.beta, load_c(p, idx)));
+  if (p.beta != 0.0f) r = __fadd_rn(r, beta_c);
   switch (p.c_type) {
     case kF32: static_cast<float*>(p.C)[idx] = r; break;
     case kBF16: static_cast<__nv_bfloat16*>(p.C)[idx] = __float2bfloat16_rn(r); break;

@@ -7,7 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/st24.h"
+#include "st24.h"
 
 namespace st24 {
 
@@ -68,16 +68,26 @@ struct StreamKPlan {
   int bm, bn, bk;          // tile shape; bk in logical K
   int64_t tiles_m, tiles_n, k_iters;
   int64_t dp_tiles, sk_tiles;
+  int64_t group_m;         // raster: tiles run in groups of group_m m-tiles, n-tile outer inside a group
   int grid;                // CTAs
+  int cluster;             // > 1: each split tile's CTAs form one cluster and reduce through DSMEM
   size_t partial_bytes;    // bytes of one fp32 partial tile
   size_t ws_bytes;         // workspace bytes (0 if no tile is split)
 };
 
 // A stream-K plan over a persistent grid of at most num_sms CTAs.
-StreamKPlan make_stream_k_plan(int bm, int bn, int bk, int64_t M, int64_t N, int64_t K, int num_sms);
+// a_row_bytes / b_col_bytes: HBM bytes of one row of A (values + metadata) and
+// of one column of B, used to pick the tile raster that keeps one operand in L2.
+// allow_cluster: the kernel can reduce split tiles inside a thread-block
+// cluster (no workspace) when every tile is split over the same 2..8 CTAs.
+StreamKPlan make_stream_k_plan(int bm, int bn, int bk, int64_t M, int64_t N, int64_t K, int num_sms,
+                               double a_row_bytes, double b_col_bytes, bool allow_cluster);
 
 // Host-side argument checks of st24_spmm (no CUDA call is made).
 st24_status check_spmm_args(const SpmmArgs& a);
+
+// The plan of the kernel family st24_spmm picks for these arguments.
+StreamKPlan plan_auto(const SpmmArgs& a, int num_sms);
 
 // The mma.sp (warp-level sparse MMA) path: every element type.
 StreamKPlan plan_spmm_mmasp(const SpmmArgs& a, int num_sms);

@@ -72,8 +72,7 @@ extern "C" st24_status st24_spmm_noalloc(st24_dtype ab_type, st24_dtype c_type, 
   if (M > 0 && N > 0 && K > 0) {
     const DeviceInfo* dev = current_device_info();
     if (!dev) return ST24_ERR_CUDA;
-    // The kernel family st24_spmm picks: tcgen05 except for int8.
-    const StreamKPlan plan = ab_type == ST24_S8 ? plan_spmm_mmasp(a, dev->num_sms) : plan_spmm_tc(a, dev->num_sms);
+    const StreamKPlan plan = plan_auto(a, dev->num_sms);   // the plan st24_spmm will use
     need = plan.ws_bytes;
     counters_at = 2 * static_cast<size_t>(plan.grid) * plan.partial_bytes;
   }

@@ -2,7 +2,7 @@
 // kernels: data-parallel waves of whole output tiles followed by a stream-K
 // tail.
 //
-// Output tiles are numbered row-major (tile = mt * tiles_n + nt).  The first
+// Output tiles are numbered in the raster of tile_coords.  The first
 // dp_tiles tiles go round-robin to the G CTAs (tile c, c + G, c + 2G, ... for
 // CTA c), so at any moment the grid works on G consecutive tiles, which keeps
 // the B panel and a few A rows hot in L2.  The remaining sk_tiles tiles are
@@ -21,6 +21,20 @@ struct Segment {
   int64_t tile;
   int64_t kb0, kb1;   // k-blocks [kb0, kb1) of the tile
 };
+
+// Output tile index -> (m-tile, n-tile): groups of group_m m-tiles, n-tile
+// outer inside a group (group_m = 1 is row-major, group_m = tiles_m is
+// column-major).
+__device__ __forceinline__ void tile_coords(int64_t tile, int64_t tiles_m, int64_t tiles_n, int64_t group_m,
+                                            int64_t& mt, int64_t& nt) {
+  const int64_t per_group = group_m * tiles_n;
+  const int64_t g = tile / per_group;
+  const int64_t first = g * group_m;
+  const int64_t rows = (tiles_m - first) < group_m ? (tiles_m - first) : group_m;
+  const int64_t i = tile - g * per_group;
+  mt = first + i % rows;
+  nt = i / rows;
+}
 
 struct Schedule {
   int64_t k_iters, dp_tiles, sk_iters, G, cta;

@@ -42,15 +42,24 @@ def call_noalloc(case, values, meta, X, Y, scale):
                                  None if scale is None else scale.data_ptr(), stream)
 
 
-@pytest.mark.parametrize("case", [inputs.decode_bf16(32), inputs.decode_bf16(1), inputs.int8(16),
-                                  inputs.spmm_case("e4m3", "f32", 1000, 40, 2048, a_std=0.02, seed=3)],
-                         ids=["bf16_N32", "bf16_N1", "int8_N16", "e4m3_ragged"])
+# Shapes whose schedule splits tiles through the scratch on both kernel families:
+# more tiles than SMs on the warp-level kernel (stream-K tail), and tcgen05 shapes.
+CASES = [
+    inputs.spmm_case("bf16", "bf16", 28672, 32, 4096, a_std=0.02, seed=1, name="bf16 28672x32x4096"),
+    inputs.spmm_case("s8", "bf16", 28672, 16, 4096, with_scale=True, seed=2, name="int8 28672x16x4096"),
+    inputs.spmm_case("bf16", "bf16", 4096, 64, 4096, a_std=0.02, seed=3, name="bf16 4096x64x4096"),
+    inputs.spmm_case("e4m3", "f32", 1000, 40, 2048, a_std=0.02, seed=4, name="e4m3 1000x40x2048"),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=["bf16_N32_streamk", "int8_N16_streamk", "bf16_N64_tcgen05",
+                                             "e4m3_ragged_tcgen05"])
 def test_noalloc_matches_spmm_twice(case):
     values, meta, X, scale = prepare(case)
     # the existing entry point with a workspace of its own
     ref = out_like(case)
     ws_bytes = st.st24_spmm_workspace_bytes(case.ab, case.c, case.M, case.N, case.K)
-    assert ws_bytes > 0   # these shapes are split over K, so the scratch is really used
+    assert ws_bytes > 0   # these shapes split tiles through the workspace, so the scratch is really used
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=DEV)
     st.st24_spmm(values, meta, X, ref, K=case.K, alpha=case.alpha, beta=case.beta, row_scale=scale, workspace=ws)
     torch.cuda.synchronize()
