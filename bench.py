@@ -81,6 +81,30 @@ def n_prune(w):
     return len(w["shapes"]) * w["layers"]
 
 
+def kernel_source_hash():
+    """sha256 of the CUDA sources and the C header (identifies the kernels a traffic figure belongs to)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "structured_sparse_gemm_gb300", "csrc", "*"))) + \
+        [os.path.join(ROOT, "include", "st24.h")]
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` on `workload` from an ncu capture recorded in
+    profiles/traffic.json, or None when absent or taken on kernels that have changed since."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[workload][kernel]
+    except Exception:
+        return None
+    return rec["dram_bytes_per_launch"] if rec.get("source_sha256") == kernel_source_hash() else None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -174,9 +198,11 @@ def prune_phase(layers, stream=None):
         st.st24_prune_compress(L["A"], L["values"], L["meta"], stream=stream)
 
 
-def spmm_phase(layers, w, stream=None, kernel="auto"):
+def spmm_phase(layers, w, stream=None, kernel="auto", only=None):
     import structured_sparse_gemm_gb300 as st
     for ni in range(len(w["Ns"])):
+        if only is not None and ni != only:
+            continue
         for L in layers:
             X, Y, ws = L["acts"][ni]
             st.st24_spmm(L["values"], L["meta"], X, Y, K=L["K"], beta=w["beta"], row_scale=L["scale"],
@@ -196,19 +222,26 @@ def run_gpu(args, w, rank, world):
         prune_phase(layers)
         spmm_phase(layers, w, kernel=args.kernel)
         stream.synchronize()
-        g_prune, g_spmm = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        # one graph for the prune phase, one per activation width for the products
+        g_prune = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_prune, stream=stream):
             prune_phase(layers)
-        with torch.cuda.graph(g_spmm, stream=stream):
-            spmm_phase(layers, w, kernel=args.kernel)
+        g_spmm = []
+        for ni in range(len(w["Ns"])):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                spmm_phase(layers, w, kernel=args.kernel, only=ni)
+            g_spmm.append(g)
     for _ in range(args.warmup):
         g_prune.replay()
-        g_spmm.replay()
+        for g in g_spmm:
+            g.replay()
     torch.cuda.synchronize()
     if st.st24_device_status() != 0:
         raise RuntimeError("device status after warm-up")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    nN = len(w["Ns"])
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + nN)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -218,8 +251,9 @@ def run_gpu(args, w, rank, world):
                 ev[k][0].record(stream)
                 g_prune.replay()
                 ev[k][1].record(stream)
-                g_spmm.replay()
-                ev[k][2].record(stream)
+                for ni, g in enumerate(g_spmm):
+                    g.replay()
+                    ev[k][2 + ni].record(stream)
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -244,14 +278,16 @@ def run_gpu(args, w, rank, world):
         nbytes = M * K * 2 + M * K // 2 * 2 + M * K // 8
         extra = {"shape": [M, K], "us_per_launch": us, "GB/s": nbytes / (us * 1e-6) / 1e9, "bytes": nbytes}
         del Wb, vb, mb
-    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    total_ms = ev[0][0].elapsed_time(ev[-1][-1])
     prune_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
-    spmm_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
+    spmm_ms = sum(e[1].elapsed_time(e[-1]) for e in ev)
+    per_n_ms = [sum(e[1 + ni].elapsed_time(e[2 + ni]) for e in ev) / args.steps for ni in range(nN)]
     status = st.st24_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    return dict(total_ms=total_ms, prune_ms=prune_ms, spmm_ms=spmm_ms, clocks=clk.summary(), extra_prune=extra,
-                layers=layers, stream=stream, g_prune=g_prune, g_spmm=g_spmm)
+    return dict(total_ms=total_ms, prune_ms=prune_ms, spmm_ms=spmm_ms, per_n_ms=per_n_ms, clocks=clk.summary(),
+                extra_prune=extra,
+                layers=layers, stream=stream)
 
 
 def run_e2e(args, w, layers, stream):
@@ -421,7 +457,8 @@ def main():
         dom = {"kernel": "st24_prune_compress", "bound": "hbm", "achieved": prune_gbs, "unit": "GB/s",
                "bytes_per_launch": prune_bytes(w) / n_prune(w), "launch_us": prune_launch_ms * 1e3}
     roofline = {"bound": dom["bound"], "achieved": dom["achieved"], "peak": hbm, "unit": "GB/s",
-                "frac": dom["achieved"] / hbm, "traffic": None, "kernel": dom["kernel"],
+                "frac": dom["achieved"] / hbm, "traffic": measured_traffic(args.workload, dom["kernel"]),
+                "kernel": dom["kernel"],
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
                 "bytes_per_launch": dom["bytes_per_launch"], "avg_launch_us": dom["launch_us"]}
 
@@ -435,6 +472,16 @@ def main():
                         "spmm": {"launches_per_step": n_spmm(w), "us_per_launch": spmm_launch_ms * 1e3,
                                  "GB/s": spmm_gbs,
                                  "tflops_dense_equiv": flops / (r["spmm_ms"] / args.steps * 1e-3) / 1e12}}}
+    per_n = {}
+    es, cs = inputs.ELEM_SIZE[w["ab"]], inputs.ELEM_SIZE[w["c"]]
+    for ni, N in enumerate(w["Ns"]):
+        us = r["per_n_ms"][ni] * 1e3 / (len(w["shapes"]) * w["layers"])
+        nbytes = sum(M * K // 2 * es + M * K // 8 + K * N * es + M * N * cs * (2 if w["beta"] else 1)
+                     for (M, K) in w["shapes"]) / len(w["shapes"])
+        fl = sum(2.0 * M * K * N for (M, K) in w["shapes"]) / len(w["shapes"])
+        per_n[str(N)] = {"us_per_launch": us, "GB/s": nbytes / (us * 1e-6) / 1e9,
+                         "tflops_dense_equiv": fl / (us * 1e-6) / 1e12}
+    line["kernels"]["spmm"]["per_N"] = per_n
     if r.get("extra_prune"):
         line["kernels"]["prune_compress_bf16"] = r["extra_prune"]
     if rank == 0 and not args.no_e2e:

@@ -79,8 +79,8 @@ typedef enum st24_status {
 
 /* Kernel families st24_spmm_ex can be asked to use. */
 typedef enum st24_kernel {
-    ST24_KERNEL_AUTO = 0,     /* what st24_spmm uses: MMA_SP for int8 and for HBM-bound N (16-bit N <= 32,
-                                 fp8 N <= 16), else TCGEN05 */
+    ST24_KERNEL_AUTO = 0,     /* what st24_spmm uses: MMA_SP for int8 and for 16-bit inputs with N <= 32
+                                 (HBM-bound), TCGEN05 otherwise (always for e4m3) */
     ST24_KERNEL_TCGEN05 = 1,  /* tcgen05.mma.sp with TMEM accumulators (f16, bf16, e4m3 only) */
     ST24_KERNEL_MMA_SP = 2    /* warp-level mma.sp (all input types) */
 } st24_kernel;

@@ -45,12 +45,13 @@ struct Traits {
   static constexpr bool kInt = DT == kS8;
 };
 
-template <int DT, int BN_, int WARPS_N_, int STAGES_>
+template <int DT, int BN_, int WARPS_N_, int STAGES_, int WMT_ = 2>
 struct Config {
   using T = Traits<DT>;
   static constexpr int BM = 128;
   static constexpr int BN = BN_;
-  static constexpr int WARPS_M = 4;
+  static constexpr int WMT = WMT_;                    // m16 tiles per warp
+  static constexpr int WARPS_M = BM / (16 * WMT_);
   static constexpr int WARPS_N = WARPS_N_;
   static constexpr int CONSUMERS = WARPS_M * WARPS_N;
   static constexpr int THREADS = (CONSUMERS + 1) * 32;
@@ -63,8 +64,14 @@ struct Config {
   static constexpr int STAGE_BYTES = (STAGE_TX + 1023) / 1024 * 1024;
   static constexpr int PARTIAL_ELEMS = BM * BN;      // one fp32/int32 partial tile
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  // Narrow (decode) tiles are sized so two CTAs fit on an SM: shared memory
+  // below half the SM's, and at most 168 registers, what the sub-partition
+  // that holds three of the two CTAs' ten warps can give (16384 / 96).
+  static constexpr bool TWO_PER_SM = BN <= 32;
+  static constexpr int MAX_REGS = TWO_PER_SM ? 168 : (THREADS > 256 ? 168 : 255);
   static_assert(WN >= 1 && BN % (8 * WARPS_N) == 0, "tile split");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  static_assert(!TWO_PER_SM || 2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
 struct Params : OutParams {
@@ -120,13 +127,15 @@ __device__ __forceinline__ void meta_words(const uint8_t* sE, int row0, int lane
   }
 }
 
-template <int DT, int BN, int WARPS_N, int STAGES>
-__global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
+template <int DT, int BN, int WARPS_N, int STAGES, int WMT>
+__global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS))
+    __maxnreg__((Config<DT, BN, WARPS_N, STAGES, WMT>::MAX_REGS))
     spmm_mmasp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmE,
                       const __grid_constant__ CUtensorMap tmB, const Params p) {
-  using Cfg = Config<DT, BN, WARPS_N, STAGES>;
+  using Cfg = Config<DT, BN, WARPS_N, STAGES, WMT>;
   using T = Traits<DT>;
   using Acc = typename std::conditional<T::kInt, int, float>::type;
+  constexpr int WROWS = WMT * 16;   // rows of a warp tile
   constexpr int WN = Cfg::WN;
 
   extern __shared__ uint8_t smem_raw[];
@@ -147,14 +156,30 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
     fence_barrier_init();
   }
   __syncthreads();
-  // Everything above overlaps the previous kernel in the stream; inputs are
-  // read only after it has completed.
-  grid_dependency_wait();
+  // Everything up to grid_dependency_wait overlaps the previous kernel in the
+  // stream.  Inputs are read only after it has completed; the producer first
+  // warms L2 with the weight tiles of its first k-blocks (an L2 prefetch
+  // cannot observe stale data), so they stream from HBM meanwhile.
   if (threadIdx.x == 0) grid_launch_dependents();
+  if (warp != Cfg::CONSUMERS) grid_dependency_wait();
 
   if (warp == Cfg::CONSUMERS) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      {
+        Schedule pre(KI, p.dp_tiles, p.sk_tiles, G, cta);
+        Segment sg;
+        int budget = STAGES;
+        while (budget > 0 && pre.next(sg)) {
+          int64_t mt, nt;
+          tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
+          for (int64_t kb = sg.kb0; kb < sg.kb1 && budget > 0; ++kb, --budget) {
+            tma_prefetch_l2_2d(&tmA, static_cast<int32_t>(kb * (128 / T::ES)), static_cast<int32_t>(mt * Cfg::BM));
+            tma_prefetch_l2_2d(&tmE, static_cast<int32_t>(kb * T::EB), static_cast<int32_t>(mt * Cfg::BM));
+          }
+        }
+      }
+      grid_dependency_wait();
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmE);
       tma_prefetch_desc(&tmB);
@@ -217,9 +242,9 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
     int64_t mt, nt;
     tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
     const int64_t m_base = mt * Cfg::BM, n_base = nt * BN;
-    Acc acc[2][WN][4];
+    Acc acc[WMT][WN][4];
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < WMT; ++i)
 #pragma unroll
       for (int j = 0; j < WN; ++j)
 #pragma unroll
@@ -232,19 +257,20 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
       const uint32_t sA = smem_u32(st);
       const uint32_t sB = smem_u32(st + Cfg::A_BYTES);
       const uint8_t* sE = st + Cfg::A_BYTES + Cfg::B_BYTES;
-      uint32_t e[2][4];
-      meta_words<DT>(sE, wm * 32, lane, p.M - m_base - wm * 32, e[0]);
-      meta_words<DT>(sE, wm * 32 + 16, lane, p.M - m_base - wm * 32 - 16, e[1]);
+      uint32_t e[WMT][4];
+#pragma unroll
+      for (int i = 0; i < WMT; ++i)
+        meta_words<DT>(sE, wm * WROWS + i * 16, lane, p.M - m_base - wm * WROWS - i * 16, e[i]);
       const int64_t ks_left = (p.K - kb * T::BK) / T::KSTEP;
       const int ksteps = ks_left < 4 ? static_cast<int>(ks_left) : 4;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         if (ks >= ksteps) break;
-        uint32_t a[2][4];
+        uint32_t a[WMT][4];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < WMT; ++i) {
           const int q = lane >> 3, r8 = lane & 7;
-          const int row = wm * 32 + i * 16 + (q & 1) * 8 + r8;
+          const int row = wm * WROWS + i * 16 + (q & 1) * 8 + r8;
           const int chunk = ks * 2 + (q >> 1);
           ldmatrix_x4(sA + row * 128 + ((chunk ^ (row & 7)) << 4), a[i][0], a[i][1], a[i][2], a[i][3]);
         }
@@ -256,7 +282,7 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
           uint32_t b[4];
           ldmatrix_x4(sB + box * (BN * 128) + n * 128 + ((cb ^ (n & 7)) << 4), b[0], b[1], b[2], b[3]);
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
+          for (int i = 0; i < WMT; ++i) {
             if constexpr (DT == kS8)
               mma_sp_16864_s8(acc[i][j], a[i], b, e[i][ks]);
             else if constexpr (DT == kE4M3)
@@ -275,9 +301,9 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
     // ---- epilogue ----
     const bool whole = (kb0 == 0 && kb1 == KI);
     bool write_out = whole;
-    bool mine[2][WN];          // fragments this CTA writes out
+    bool mine[WMT][WN];        // fragments this CTA writes out
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < WMT; ++i)
 #pragma unroll
       for (int j = 0; j < WN; ++j) mine[i][j] = true;
     if (!whole && p.cluster > 1) {
@@ -290,10 +316,10 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
       consumer_sync(Cfg::CONSUMERS * 32);
       float4* part = reinterpret_cast<float4*>(smem);
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < WMT; ++i)
 #pragma unroll
         for (int j = 0; j < WN; ++j) {
-          const int f = (warp * 2 + i) * WN + j;
+          const int f = (warp * WMT + i) * WN + j;
           if constexpr (T::kInt)
             part[f * 32 + lane] = make_float4(__int_as_float(acc[i][j][0]), __int_as_float(acc[i][j][1]),
                                               __int_as_float(acc[i][j][2]), __int_as_float(acc[i][j][3]));
@@ -304,29 +330,31 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
       cluster_done = 1;
       const int rank = static_cast<int>(cluster_ctarank());
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < WMT; ++i)
 #pragma unroll
         for (int j = 0; j < WN; ++j) {
-          const int f = (warp * 2 + i) * WN + j;
+          const int f = (warp * WMT + i) * WN + j;
           mine[i][j] = (f % p.cluster) == rank;
           if (!mine[i][j]) continue;
-          float4 v[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            if (q < p.cluster) v[q] = ld_shared_cluster_f4(part + f * 32 + lane, static_cast<uint32_t>(q));
           Acc t[4];
+          for (int q0 = 0; q0 < p.cluster; q0 += 4) {   // ranks in order, 4 loads in flight
+            float4 v[4];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            if (q >= p.cluster) break;
-            Acc u[4];
-            if constexpr (T::kInt) {
-              u[0] = __float_as_int(v[q].x); u[1] = __float_as_int(v[q].y);
-              u[2] = __float_as_int(v[q].z); u[3] = __float_as_int(v[q].w);
-            } else {
-              u[0] = v[q].x; u[1] = v[q].y; u[2] = v[q].z; u[3] = v[q].w;
+            for (int u = 0; u < 4; ++u)
+              if (q0 + u < p.cluster) v[u] = ld_shared_cluster_f4(part + f * 32 + lane, static_cast<uint32_t>(q0 + u));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (q0 + u >= p.cluster) break;
+              Acc w[4];
+              if constexpr (T::kInt) {
+                w[0] = __float_as_int(v[u].x); w[1] = __float_as_int(v[u].y);
+                w[2] = __float_as_int(v[u].z); w[3] = __float_as_int(v[u].w);
+              } else {
+                w[0] = v[u].x; w[1] = v[u].y; w[2] = v[u].z; w[3] = v[u].w;
+              }
+#pragma unroll
+              for (int r = 0; r < 4; ++r) t[r] = (q0 + u == 0) ? w[r] : t[r] + w[r];
             }
-#pragma unroll
-            for (int r = 0; r < 4; ++r) t[r] = (q == 0) ? u[r] : t[r] + u[r];
           }
 #pragma unroll
           for (int r = 0; r < 4; ++r) acc[i][j][r] = t[r];
@@ -339,10 +367,10 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
       auto slot_of = [&](int64_t c) -> int64_t { return sch.slot(c, tile); };
       float4* mine = reinterpret_cast<float4*>(p.partials + slot_of(cta) * Cfg::PARTIAL_ELEMS);
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < WMT; ++i)
 #pragma unroll
         for (int j = 0; j < WN; ++j) {
-          const int idx = ((warp * 2 + i) * WN + j) * 32 + lane;
+          const int idx = ((warp * WMT + i) * WN + j) * 32 + lane;
           float4 v;
           if constexpr (T::kInt) {
             v = make_float4(__int_as_float(acc[i][j][0]), __int_as_float(acc[i][j][1]),
@@ -369,9 +397,9 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
         // fragments are loaded as one batch of independent loads, so a segment
         // costs one memory latency; this CTA's own partial comes from registers.
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < WMT; ++i) {
           Acc t[WN][4];
-          constexpr int U = WN <= 4 ? 4 : 1;   // segments whose loads are issued together
+          constexpr int U = WN >= 4 ? 1 : 4 / WN;   // segments whose loads are issued together
           for (int64_t cb = c_lo; cb <= c_hi; cb += U) {
             float4 f[U][WN];
 #pragma unroll
@@ -379,7 +407,7 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
               if (cb + u <= c_hi && cb + u != cta) {
                 const float4* src = reinterpret_cast<const float4*>(p.partials + slot_of(cb + u) * Cfg::PARTIAL_ELEMS);
 #pragma unroll
-                for (int j = 0; j < WN; ++j) f[u][j] = __ldcg(src + ((warp * 2 + i) * WN + j) * 32 + lane);
+                for (int j = 0; j < WN; ++j) f[u][j] = __ldcg(src + ((warp * WMT + i) * WN + j) * 32 + lane);
               }
             }
 #pragma unroll
@@ -411,28 +439,26 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
       }
     }
     if (write_out) {
-      // All of this thread's C inputs are read before any output is written.
+      // A fragment's four C inputs are read before its four outputs are written.
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        float bc[WN][4];
+      for (int i = 0; i < WMT; ++i)
 #pragma unroll
-        for (int j = 0; j < WN; ++j)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int64_t m = m_base + wm * 32 + i * 16 + gid + 8 * (r >> 1);
-            const int64_t n = n_base + wn * WN * 8 + j * 8 + 2 * tig + (r & 1);
-            bc[j][r] = (mine[i][j] && m < p.M && n < p.N) ? load_beta_c(p, m, n) : 0.0f;
-          }
-#pragma unroll
-        for (int j = 0; j < WN; ++j)
+        for (int j = 0; j < WN; ++j) {
+          if (!mine[i][j]) continue;
+          float bc[4];
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
-            const int64_t m = m_base + wm * 32 + i * 16 + gid + 8 * (r >> 1);
+            const int64_t m = m_base + wm * WROWS + i * 16 + gid + 8 * (r >> 1);
             const int64_t n = n_base + wn * WN * 8 + j * 8 + 2 * tig + (r & 1);
-            if (mine[i][j] && m < p.M && n < p.N)
-              store_out<Acc>(p, m, n, acc[i][j][r], row_factor(p, m), bc[j][r]);
+            bc[r] = (m < p.M && n < p.N) ? load_beta_c(p, m, n) : 0.0f;
           }
-      }
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int64_t m = m_base + wm * WROWS + i * 16 + gid + 8 * (r >> 1);
+            const int64_t n = n_base + wn * WN * 8 + j * 8 + 2 * tig + (r & 1);
+            if (m < p.M && n < p.N) store_out<Acc>(p, m, n, acc[i][j][r], row_factor(p, m), bc[r]);
+          }
+        }
     }
     if (cluster_done == 1) {
       cluster_sync();   // peers have finished reading this CTA's shared memory
@@ -448,10 +474,10 @@ __global__ void __launch_bounds__(Config<DT, BN, WARPS_N, STAGES>::THREADS, 1)
     }
 }
 
-template <int DT, int BN, int WARPS_N, int STAGES>
+template <int DT, int BN, int WARPS_N, int STAGES, int WMT = 2>
 st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev,
                        cudaStream_t stream) {
-  using Cfg = Config<DT, BN, WARPS_N, STAGES>;
+  using Cfg = Config<DT, BN, WARPS_N, STAGES, WMT>;
   using T = Traits<DT>;
   const CUtensorMapDataType ty = T::ES == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   CUtensorMap tmA, tmE, tmB;
@@ -482,7 +508,7 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
                                                  2 * static_cast<size_t>(plan.grid) * plan.partial_bytes)
                    : nullptr;
   p.status = dev.status;
-  auto kern = spmm_mmasp_kernel<DT, BN, WARPS_N, STAGES>;
+  auto kern = spmm_mmasp_kernel<DT, BN, WARPS_N, STAGES, WMT>;
   static bool attr_set[64] = {};
   if (!attr_set[dev.device % 64]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
@@ -520,9 +546,9 @@ st24_status launch_dt_impl(const SpmmArgs& a, const StreamKPlan& plan, const Dev
                       cudaStream_t s) {
   constexpr bool k16 = Traits<DT>::ES == 2;
   switch (plan.bn) {
-    case 8: return launch_cfg<DT, 8, 1, 8>(a, plan, dev, s);
-    case 16: return launch_cfg<DT, 16, 1, 8>(a, plan, dev, s);
-    case 32: return launch_cfg<DT, 32, 1, k16 ? 7 : 6>(a, plan, dev, s);
+    case 8: return launch_cfg<DT, 8, 1, 5>(a, plan, dev, s);
+    case 16: return launch_cfg<DT, 16, 1, k16 ? 5 : 4>(a, plan, dev, s);
+    case 32: return launch_cfg<DT, 32, 1, k16 ? 4 : 3>(a, plan, dev, s);
     case 64: return launch_cfg<DT, 64, 1, k16 ? 6 : 5>(a, plan, dev, s);
     default: return launch_cfg<DT, 128, 2, 4>(a, plan, dev, s);
   }

@@ -134,14 +134,30 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // The prologue above overlaps the previous kernel in the stream; inputs are
-  // read only after it has completed.
-  grid_dependency_wait();
+  // Everything up to grid_dependency_wait overlaps the previous kernel in the
+  // stream.  Inputs are read only after it has completed; the producer first
+  // warms L2 with the weight tiles of its first k-blocks (an L2 prefetch
+  // cannot observe stale data), so they stream from HBM meanwhile.
   if (threadIdx.x == 0) grid_launch_dependents();
+  if (warp != 0) grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      {
+        Schedule pre(KI, p.dp_tiles, p.sk_tiles, G, cta);
+        Segment sg;
+        int budget = STAGES;
+        while (budget > 0 && pre.next(sg)) {
+          int64_t mt, nt;
+          tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
+          for (int64_t kb = sg.kb0; kb < sg.kb1 && budget > 0; ++kb, --budget) {
+            tma_prefetch_l2_2d(&tmA, static_cast<int32_t>(kb * (128 / T::ES)), static_cast<int32_t>(mt * Cfg::BM));
+            tma_prefetch_l2_2d(&tmE, static_cast<int32_t>(kb * T::EB), static_cast<int32_t>(mt * Cfg::BM));
+          }
+        }
+      }
+      grid_dependency_wait();
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmE);
       tma_prefetch_desc(&tmB);

@@ -143,14 +143,18 @@ namespace {
 
 // The kernel family a call runs on: tcgen05 for the 16-bit and fp8 inputs,
 // the warp-level sparse MMA for int8 (there is no int8 tcgen05 kind on sm_103a).
-// Products whose arithmetic intensity is low enough to be bound by streaming
-// the compressed A from HBM (2N flops per logical weight over s/2 + 1/8 bytes,
-// at most 64 flop/B: N <= 32 for 16-bit inputs, N <= 16 for fp8) run on the
-// warp-level kernel, which has less fixed latency per launch (measured);
-// int8 always does (no int8 tcgen05 kind on sm_103a); the rest run on tcgen05.
+// Which kernel family st24_spmm uses (measured on GB300):
+//  * int8: the warp-level kernel (there is no int8 tcgen05 kind on sm_103a).
+//  * fp8: tcgen05 always; the warp-level e4m3 sparse MMA runs at ~1/50 of the
+//    16-bit one on this GPU.
+//  * 16-bit: the warp-level kernel while the product is bound by streaming
+//    the compressed A from HBM (2N flops per logical weight over 1.125 bytes,
+//    at most 64 flop/B: N <= 32), where it has less fixed latency per launch;
+//    tcgen05 beyond.
 int resolve_kernel(int requested, int ab, int64_t N) {
   if (requested != ST24_KERNEL_AUTO) return requested;
   if (ab == kS8) return ST24_KERNEL_MMA_SP;
+  if (ab == kE4M3) return ST24_KERNEL_TCGEN05;
   const double intensity = 2.0 * static_cast<double>(N) / (elem_size(ab) / 2.0 + 0.125);
   return intensity <= 64.0 ? ST24_KERNEL_MMA_SP : ST24_KERNEL_TCGEN05;
 }
