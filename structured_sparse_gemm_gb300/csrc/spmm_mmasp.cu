@@ -21,7 +21,7 @@ using namespace mmasp;
 StreamKPlan plan_spmm_mmasp(const SpmmArgs& a, int num_sms) {
   return make_stream_k_plan(128, pick_bn(a.N), elem_size(a.ab) == 2 ? 128 : 256, a.M, a.N, a.K, num_sms,
                             a.K * (elem_size(a.ab) / 2.0 + 0.125), static_cast<double>(a.K) * elem_size(a.ab),
-                            true);
+                            /*allow_cluster=*/pick_bn(a.N) <= 64);
 }
 
 st24_status launch_scale_c(const SpmmArgs& a, const DeviceInfo& dev, cudaStream_t stream) {

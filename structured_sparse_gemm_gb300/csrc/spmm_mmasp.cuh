@@ -63,7 +63,11 @@ struct Config {
   static constexpr int STAGE_TX = A_BYTES + B_BYTES + E_BYTES;
   static constexpr int STAGE_BYTES = (STAGE_TX + 1023) / 1024 * 1024;
   static constexpr int PARTIAL_ELEMS = BM * BN;      // one fp32/int32 partial tile
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  // In-cluster split-K: partial fragments pushed by the cluster's CTAs land
+  // here (a region of its own, so no CTA has to wait for another to leave
+  // its main loop before pushing).
+  static constexpr int PUSH_BYTES = BN <= 64 ? BM * BN * 4 : 0;   // wide tiles never run in cluster mode
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + PUSH_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   // Narrow (decode) tiles are sized so two CTAs fit on an SM: shared memory
   // below half the SM's, and at most 168 registers, what the sub-partition
   // that holds three of the two CTAs' ten warps can give (16384 / 96).
@@ -140,7 +144,8 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE_BYTES);
+  float4* push_slots = reinterpret_cast<float4*>(smem + STAGES * Cfg::STAGE_BYTES);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE_BYTES + Cfg::PUSH_BYTES);
   uint64_t* empty_bar = full_bar + STAGES;
   int* s_last = reinterpret_cast<int*>(empty_bar + STAGES);
 
@@ -220,18 +225,13 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
         if (issued[s]) mbar_wait(smem_u32(&full_bar[s]), issued_parity[s], p.status);
     }
     __syncwarp();
-    if (p.cluster > 1) {
-      // The producer warp takes part in the two cluster barriers of the
-      // in-cluster reduction (see the consumers).
-      cluster_sync();
-      cluster_sync();
-    }
+    if (p.cluster > 1) cluster_sync();   // the producer warp's part in the in-cluster reduction
     return;
   }
 
   // -------------------------------------------------------------- consumers
   const int wm = warp % Cfg::WARPS_M, wn = warp / Cfg::WARPS_M;
-  int cluster_done = 0;   // cluster barriers passed (cluster mode: exactly two per CTA)
+  int cluster_done = 0;   // cluster barrier phases passed (cluster mode: exactly one per CTA)
   const int gid = lane >> 2, tig = lane & 3;
   int stage = 0;
   uint32_t phase = 0;
@@ -308,53 +308,52 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
       for (int j = 0; j < WN; ++j) mine[i][j] = true;
     if (!whole && p.cluster > 1) {
       // Split-K inside the cluster: CTA rank r of the cluster holds the r-th
-      // k-range of this tile.  Every CTA parks its fragments in its own shared
-      // memory (the stage ring, idle now); after a cluster barrier each CTA
-      // sums a 1/cluster share of the fragments over the ranks in order and
-      // writes it out; a second barrier keeps the memory alive until all
-      // peers have read it.
-      consumer_sync(Cfg::CONSUMERS * 32);
-      float4* part = reinterpret_cast<float4*>(smem);
+      // k-range of this tile.  Fragment f of the tile is finished by CTA
+      // f % cluster; every CTA pushes its partial of f straight into that
+      // CTA's push region, slot [r][f / cluster].  One cluster barrier makes
+      // the pushes visible; each CTA then sums its own fragments over the
+      // ranks in order (k order) from local memory and writes them out.  No
+      // CTA touches another's memory after the barrier, so none waits for the
+      // others before exiting.
+      constexpr int F = Cfg::CONSUMERS * WMT * WN;            // fragments of the tile
+      const int cs = p.cluster;
+      const int owned_max = (F + cs - 1) / cs;
+      const int rank = static_cast<int>(cluster_ctarank());
+      float4* slots = push_slots;                            // [cluster][owned_max][32 lanes]
 #pragma unroll
       for (int i = 0; i < WMT; ++i)
 #pragma unroll
         for (int j = 0; j < WN; ++j) {
           const int f = (warp * WMT + i) * WN + j;
+          float4 v;
           if constexpr (T::kInt)
-            part[f * 32 + lane] = make_float4(__int_as_float(acc[i][j][0]), __int_as_float(acc[i][j][1]),
-                                              __int_as_float(acc[i][j][2]), __int_as_float(acc[i][j][3]));
+            v = make_float4(__int_as_float(acc[i][j][0]), __int_as_float(acc[i][j][1]),
+                            __int_as_float(acc[i][j][2]), __int_as_float(acc[i][j][3]));
           else
-            part[f * 32 + lane] = make_float4(acc[i][j][0], acc[i][j][1], acc[i][j][2], acc[i][j][3]);
+            v = make_float4(acc[i][j][0], acc[i][j][1], acc[i][j][2], acc[i][j][3]);
+          st_shared_cluster_f4(slots + (rank * owned_max + f / cs) * 32 + lane, static_cast<uint32_t>(f % cs), v);
         }
       cluster_sync();
       cluster_done = 1;
-      const int rank = static_cast<int>(cluster_ctarank());
 #pragma unroll
       for (int i = 0; i < WMT; ++i)
 #pragma unroll
         for (int j = 0; j < WN; ++j) {
           const int f = (warp * WMT + i) * WN + j;
-          mine[i][j] = (f % p.cluster) == rank;
+          mine[i][j] = (f % cs) == rank;
           if (!mine[i][j]) continue;
           Acc t[4];
-          for (int q0 = 0; q0 < p.cluster; q0 += 4) {   // ranks in order, 4 loads in flight
-            float4 v[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (q0 + u < p.cluster) v[u] = ld_shared_cluster_f4(part + f * 32 + lane, static_cast<uint32_t>(q0 + u));
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              if (q0 + u >= p.cluster) break;
-              Acc w[4];
-              if constexpr (T::kInt) {
-                w[0] = __float_as_int(v[u].x); w[1] = __float_as_int(v[u].y);
-                w[2] = __float_as_int(v[u].z); w[3] = __float_as_int(v[u].w);
-              } else {
-                w[0] = v[u].x; w[1] = v[u].y; w[2] = v[u].z; w[3] = v[u].w;
-              }
-#pragma unroll
-              for (int r = 0; r < 4; ++r) t[r] = (q0 + u == 0) ? w[r] : t[r] + w[r];
+          for (int q = 0; q < cs; ++q) {
+            const float4 v = slots[(q * owned_max + f / cs) * 32 + lane];
+            Acc w[4];
+            if constexpr (T::kInt) {
+              w[0] = __float_as_int(v.x); w[1] = __float_as_int(v.y);
+              w[2] = __float_as_int(v.z); w[3] = __float_as_int(v.w);
+            } else {
+              w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
             }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) t[r] = (q == 0) ? w[r] : t[r] + w[r];
           }
 #pragma unroll
           for (int r = 0; r < 4; ++r) acc[i][j][r] = t[r];
@@ -460,18 +459,10 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
           }
         }
     }
-    if (cluster_done == 1) {
-      cluster_sync();   // peers have finished reading this CTA's shared memory
-      cluster_done = 2;
-    }
   }
   // A wait that ran out of time skipped the reduction: still meet the peers
-  // at both cluster barriers.
-  if (p.cluster > 1)
-    while (cluster_done < 2) {
-      cluster_sync();
-      ++cluster_done;
-    }
+  // at the cluster barrier.
+  if (p.cluster > 1 && cluster_done == 0) cluster_sync();
 }
 
 template <int DT, int BN, int WARPS_N, int STAGES, int WMT = 2>
@@ -546,10 +537,10 @@ st24_status launch_dt_impl(const SpmmArgs& a, const StreamKPlan& plan, const Dev
                       cudaStream_t s) {
   constexpr bool k16 = Traits<DT>::ES == 2;
   switch (plan.bn) {
-    case 8: return launch_cfg<DT, 8, 1, 5>(a, plan, dev, s);
-    case 16: return launch_cfg<DT, 16, 1, k16 ? 5 : 4>(a, plan, dev, s);
-    case 32: return launch_cfg<DT, 32, 1, k16 ? 4 : 3>(a, plan, dev, s);
-    case 64: return launch_cfg<DT, 64, 1, k16 ? 6 : 5>(a, plan, dev, s);
+    case 8: return launch_cfg<DT, 8, 1, k16 ? 5 : 4>(a, plan, dev, s);
+    case 16: return launch_cfg<DT, 16, 1, 4>(a, plan, dev, s);
+    case 32: return launch_cfg<DT, 32, 1, 3>(a, plan, dev, s);
+    case 64: return launch_cfg<DT, 64, 1, 5>(a, plan, dev, s);
     default: return launch_cfg<DT, 128, 2, 4>(a, plan, dev, s);
   }
 }

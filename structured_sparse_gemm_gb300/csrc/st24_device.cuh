@@ -298,6 +298,15 @@ __device__ __forceinline__ float4 ld_shared_cluster_f4(const void* local, uint32
                : "memory");
   return v;
 }
+// A 16-byte store to the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ void st_shared_cluster_f4(void* local, uint32_t rank, float4 v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+
 // Wait for the grids this one depends on (programmatic dependent launch);
 // a no-op when the kernel was not launched as a dependent.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
