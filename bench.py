@@ -56,21 +56,25 @@ def flops_per_step(w):
 
 def spmm_bytes(w):
     """Algorithmic HBM bytes of all SpMM launches of one step (compressed A, B, C, scale)."""
-    es = inputs.ELEM_SIZE[w["ab"]]
-    cs = inputs.ELEM_SIZE[w["c"]]
-    total = 0
-    for (M, K) in w["shapes"]:
-        for N in w["Ns"]:
-            b = M * K // 2 * es + M * K // 8 + K * N * es + M * N * cs * (2 if w["beta"] else 1)
-            if w["scale"]:
-                b += 4 * M
-            total += b
-    return total * w["layers"]
+    return sum(launch_bytes(w, M, K, N) for (M, K) in w["shapes"] for N in w["Ns"]) * w["layers"]
 
 
 def prune_bytes(w):
     es = inputs.ELEM_SIZE[w["ab"]]
     return sum(M * K * es + M * K // 2 * es + M * K // 8 for (M, K) in w["shapes"]) * w["layers"]
+
+
+def groups(w):
+    """(activation index, shape index) pairs, one captured graph and one timing each."""
+    return [(ni, si) for ni in range(len(w["Ns"])) for si in range(len(w["shapes"]))]
+
+
+def launch_bytes(w, M, K, N):
+    """Algorithmic HBM bytes of one product: compressed A and metadata, B, C (read too when beta != 0), scale."""
+    es = inputs.ELEM_SIZE[w["ab"]]
+    cs = inputs.ELEM_SIZE[w["c"]]
+    return M * K // 2 * es + M * K // 8 + K * N * es + M * N * cs * (2 if w["beta"] else 1) + \
+        (4 * M if w["scale"] else 0)
 
 
 def n_spmm(w):
@@ -86,8 +90,8 @@ def kernel_source_hash():
     import glob
     import hashlib
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "structured_sparse_gemm_gb300", "csrc", "*"))) + \
-        [os.path.join(ROOT, "include", "st24.h")]
+    files = sorted(f for f in glob.glob(os.path.join(ROOT, "structured_sparse_gemm_gb300", "csrc", "*"))
+                   if os.path.isfile(f)) + [os.path.join(ROOT, "include", "st24.h")]
     for f in files:
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode() + b"\0" + fh.read())
@@ -113,6 +117,36 @@ def peaks():
         return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
     except Exception:
         return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def mma_sp_peak_tops(kind: int) -> float | None:
+    """Dense-equivalent TOPS of back-to-back register-only mma.sp (kind 0: int8
+    m16n8k64, 1: bf16 m16n8k32), measured now on this GPU by the library's
+    peak probe; None if it cannot run."""
+    import ctypes
+    import structured_sparse_gemm_gb300 as st
+    try:
+        lib = ctypes.CDLL(st._build_lib.PEAK_LIB)
+        lib.st24peak_mma_sp.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
+        out = ctypes.c_double(0.0)
+        return out.value if lib.st24peak_mma_sp(kind, ctypes.byref(out)) == 0 else None
+    except OSError:
+        return None
+
+
+def tensor_peak(ab: str, bf16_dense: float):
+    """2:4-sparse tensor peak (dense-equivalent TFLOP/s) of an element type, and where it comes from.
+
+    16-bit: twice the measured dense bf16 peak; e4m3: twice that again (the nominal
+    fp8/bf16 ratio); int8: the measured mma.sp rate (tcgen05 has no int8 kind here)."""
+    if ab in ("bf16", "f16"):
+        return 2.0 * bf16_dense, "2 x measured dense bf16 (MEASURED_PEAKS.json bf16_tflops)"
+    if ab == "e4m3":
+        return 4.0 * bf16_dense, "4 x measured dense bf16 (sparse x2, fp8/bf16 nominal x2)"
+    t = mma_sp_peak_tops(0)
+    if t is None:
+        return None, "unavailable"
+    return t, "measured live: register-only mma.sp m16n8k64 s8 loop (csrc/peak/peak_mma_sp.cu)"
 
 
 # ---------------------------------------------------------------- clocks
@@ -188,7 +222,7 @@ def build_workload(w, dev, seed=0):
                 ws_bytes = st.st24_spmm_workspace_bytes(w["ab"], w["c"], M, N, K)
                 ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
                 acts.append((X, Y, ws))
-            layers.append(dict(A=A, values=values, meta=meta, scale=scale, acts=acts, M=M, K=K))
+            layers.append(dict(A=A, values=values, meta=meta, scale=scale, acts=acts, M=M, K=K, si=si))
     return layers
 
 
@@ -198,15 +232,18 @@ def prune_phase(layers, stream=None):
         st.st24_prune_compress(L["A"], L["values"], L["meta"], stream=stream)
 
 
-def spmm_phase(layers, w, stream=None, kernel="auto", only=None):
+def spmm_phase(layers, w, stream=None, kernel="auto", only=None, fixed_a=True):
+    """The products of one step.  Run inside a captured graph, after the prune
+    graph has completed, so the weights are fixed for the whole phase
+    (ST24_SPMM_FIXED_A)."""
     import structured_sparse_gemm_gb300 as st
     for ni in range(len(w["Ns"])):
-        if only is not None and ni != only:
-            continue
         for L in layers:
+            if only is not None and (ni, L["si"]) != only:
+                continue
             X, Y, ws = L["acts"][ni]
             st.st24_spmm(L["values"], L["meta"], X, Y, K=L["K"], beta=w["beta"], row_scale=L["scale"],
-                         workspace=ws, stream=stream, kernel=kernel)
+                         workspace=ws, stream=stream, kernel=kernel, fixed_a=fixed_a)
 
 
 def run_gpu(args, w, rank, world):
@@ -220,17 +257,17 @@ def run_gpu(args, w, rank, world):
     with torch.cuda.stream(stream):
         # eager warm-up (also sets kernel attributes before capture)
         prune_phase(layers)
-        spmm_phase(layers, w, kernel=args.kernel)
+        spmm_phase(layers, w, kernel=args.kernel, fixed_a=args.fixed_a)
         stream.synchronize()
         # one graph for the prune phase, one per activation width for the products
         g_prune = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_prune, stream=stream):
             prune_phase(layers)
         g_spmm = []
-        for ni in range(len(w["Ns"])):
+        for grp in groups(w):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                spmm_phase(layers, w, kernel=args.kernel, only=ni)
+                spmm_phase(layers, w, kernel=args.kernel, only=grp, fixed_a=args.fixed_a)
             g_spmm.append(g)
     for _ in range(args.warmup):
         g_prune.replay()
@@ -240,8 +277,8 @@ def run_gpu(args, w, rank, world):
     if st.st24_device_status() != 0:
         raise RuntimeError("device status after warm-up")
 
-    nN = len(w["Ns"])
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + nN)] for _ in range(args.steps)]
+    nG = len(groups(w))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + nG)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -281,11 +318,11 @@ def run_gpu(args, w, rank, world):
     total_ms = ev[0][0].elapsed_time(ev[-1][-1])
     prune_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
     spmm_ms = sum(e[1].elapsed_time(e[-1]) for e in ev)
-    per_n_ms = [sum(e[1 + ni].elapsed_time(e[2 + ni]) for e in ev) / args.steps for ni in range(nN)]
+    per_group_ms = [sum(e[1 + gi].elapsed_time(e[2 + gi]) for e in ev) / args.steps for gi in range(nG)]
     status = st.st24_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    return dict(total_ms=total_ms, prune_ms=prune_ms, spmm_ms=spmm_ms, per_n_ms=per_n_ms, clocks=clk.summary(),
+    return dict(total_ms=total_ms, prune_ms=prune_ms, spmm_ms=spmm_ms, per_group_ms=per_group_ms, clocks=clk.summary(),
                 extra_prune=extra,
                 layers=layers, stream=stream)
 
@@ -319,10 +356,13 @@ def run_e2e(args, w, layers, stream):
             for L in layers:
                 st.st24_prune_compress(L["A"], L["values"], L["meta"])
             for ni in range(len(w["Ns"])):
-                for L in layers:
+                for li, L in enumerate(layers):
                     X, Y, ws = L["acts"][ni]
+                    # The weights pruned by the kernel just before the first
+                    # product may still be in flight: that product waits.
+                    fixed = args.fixed_a and not (ni == 0 and li == 0 and len(layers) == 1)
                     st.st24_spmm(L["values"], L["meta"], X, Y, K=L["K"], beta=w["beta"], row_scale=L["scale"],
-                                 workspace=ws)
+                                 workspace=ws, fixed_a=fixed)
             for L, (hA, hX) in zip(layers, host):
                 for (X, Y, ws), (hx, hy) in zip(L["acts"], hX):
                     hy.copy_(Y, non_blocking=True)
@@ -400,6 +440,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kernel", default="auto", choices=["auto", "tcgen05", "mma_sp"],
                     help="SpMM kernel family (auto = what st24_spmm picks)")
+    ap.add_argument("--no-fixed-a", dest="fixed_a", action="store_false",
+                    help="do not declare the weights fixed (ST24_SPMM_FIXED_A) to the products")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
 
@@ -408,7 +450,7 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
     config = {"workload": w["desc"], "name": args.workload, "kernel": args.kernel, "shapes": w["shapes"], "Ns": w["Ns"],
-              "layers": w["layers"], "ab": w["ab"], "out": w["c"],
+              "layers": w["layers"], "ab": w["ab"], "out": w["c"], "fixed_a": args.fixed_a,
               "l2": "inputs larger than L2: every step streams all weights (dense and compressed) from HBM"}
 
     if args.impl == "reference":
@@ -449,18 +491,53 @@ def main():
     prune_launch_ms = r["prune_ms"] / args.steps / n_prune(w)
     spmm_gbs = spmm_bytes(w) / (r["spmm_ms"] / args.steps * 1e-3) / 1e9
     prune_gbs = prune_bytes(w) / (r["prune_ms"] / args.steps * 1e-3) / 1e9
-    # dominant kernel by share of the step
+    tpeak, tpeak_src = tensor_peak(w["ab"], bf16_peak)
+    hbm_src = f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback"
+
+    # Every (shape, N) product group: its bound is the one its arithmetic
+    # intensity meets first (flops / tensor peak vs bytes / HBM peak).
+    per_group = []
+    for gi, (ni, si) in enumerate(groups(w)):
+        (M, K), N = w["shapes"][si], w["Ns"][ni]
+        us = r["per_group_ms"][gi] * 1e3 / w["layers"]
+        nbytes = launch_bytes(w, M, K, N)
+        fl = 2.0 * M * K * N
+        tensor_bound = tpeak is not None and fl / (tpeak * 1e12) > nbytes / (hbm * 1e9)
+        g = {"M": M, "K": K, "N": N, "launches_per_step": w["layers"], "us_per_launch": us,
+             "bytes_per_launch": nbytes, "GB/s": nbytes / (us * 1e-6) / 1e9,
+             "tflops_dense_equiv": fl / (us * 1e-6) / 1e12, "tflops_actual": fl / 2 / (us * 1e-6) / 1e12,
+             "bound": "tensor" if tensor_bound else "hbm"}
+        g["frac"] = g["tflops_dense_equiv"] / tpeak if tensor_bound else g["GB/s"] / hbm
+        g["share_of_step"] = r["per_group_ms"][gi] / (r["total_ms"] / args.steps)
+        per_group.append(g)
+
+    # The dominant kernel (the products or the prune, by share of the step).
+    # For the products: the launches of the bound that takes most of their
+    # time, aggregated (algorithmic bytes or flops over their summed time).
     if r["spmm_ms"] >= r["prune_ms"]:
-        dom = {"kernel": "st24_spmm", "bound": "hbm", "achieved": spmm_gbs, "unit": "GB/s",
-               "bytes_per_launch": spmm_bytes(w) / n_spmm(w), "launch_us": spmm_launch_ms * 1e3}
+        by_bound = {}
+        for g in per_group:
+            by_bound.setdefault(g["bound"], []).append(g)
+        bound = max(by_bound, key=lambda b: sum(g["us_per_launch"] * g["launches_per_step"] for g in by_bound[b]))
+        sel = by_bound[bound]
+        t_s = sum(g["us_per_launch"] * g["launches_per_step"] for g in sel) * 1e-6
+        n_l = sum(g["launches_per_step"] for g in sel)
+        label = "st24_spmm " + ", ".join(f"{g['M']}x{g['K']} N={g['N']}" for g in sel)
+        if bound == "tensor":
+            fl = sum(2.0 * g["M"] * g["K"] * g["N"] * g["launches_per_step"] for g in sel)
+            roofline = {"bound": "tensor", "achieved": fl / t_s / 1e12, "peak": tpeak, "unit": "TFLOP/s",
+                        "frac": fl / t_s / 1e12 / tpeak, "peak_source": tpeak_src, "flops_per_launch": fl / n_l}
+        else:
+            nb = sum(g["bytes_per_launch"] * g["launches_per_step"] for g in sel)
+            roofline = {"bound": "hbm", "achieved": nb / t_s / 1e9, "peak": hbm, "unit": "GB/s",
+                        "frac": nb / t_s / 1e9 / hbm, "peak_source": hbm_src, "bytes_per_launch": nb / n_l}
+        roofline.update({"traffic": measured_traffic(args.workload, "st24_spmm"), "kernel": label,
+                         "avg_launch_us": t_s * 1e6 / n_l})
     else:
-        dom = {"kernel": "st24_prune_compress", "bound": "hbm", "achieved": prune_gbs, "unit": "GB/s",
-               "bytes_per_launch": prune_bytes(w) / n_prune(w), "launch_us": prune_launch_ms * 1e3}
-    roofline = {"bound": dom["bound"], "achieved": dom["achieved"], "peak": hbm, "unit": "GB/s",
-                "frac": dom["achieved"] / hbm, "traffic": measured_traffic(args.workload, dom["kernel"]),
-                "kernel": dom["kernel"],
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-                "bytes_per_launch": dom["bytes_per_launch"], "avg_launch_us": dom["launch_us"]}
+        roofline = {"bound": "hbm", "achieved": prune_gbs, "peak": hbm, "unit": "GB/s", "frac": prune_gbs / hbm,
+                    "traffic": measured_traffic(args.workload, "st24_prune_compress"),
+                    "kernel": "st24_prune_compress", "peak_source": hbm_src,
+                    "bytes_per_launch": prune_bytes(w) / n_prune(w), "avg_launch_us": prune_launch_ms * 1e3}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -468,20 +545,12 @@ def main():
             "gpu_launches": args.steps * (n_spmm(w) + n_prune(w)),
             "clocks": r["clocks"], "roofline": roofline,
             "kernels": {"prune_compress": {"launches_per_step": n_prune(w), "us_per_launch": prune_launch_ms * 1e3,
-                                           "GB/s": prune_gbs},
+                                           "GB/s": prune_gbs, "frac_hbm": prune_gbs / hbm},
                         "spmm": {"launches_per_step": n_spmm(w), "us_per_launch": spmm_launch_ms * 1e3,
                                  "GB/s": spmm_gbs,
-                                 "tflops_dense_equiv": flops / (r["spmm_ms"] / args.steps * 1e-3) / 1e12}}}
-    per_n = {}
-    es, cs = inputs.ELEM_SIZE[w["ab"]], inputs.ELEM_SIZE[w["c"]]
-    for ni, N in enumerate(w["Ns"]):
-        us = r["per_n_ms"][ni] * 1e3 / (len(w["shapes"]) * w["layers"])
-        nbytes = sum(M * K // 2 * es + M * K // 8 + K * N * es + M * N * cs * (2 if w["beta"] else 1)
-                     for (M, K) in w["shapes"]) / len(w["shapes"])
-        fl = sum(2.0 * M * K * N for (M, K) in w["shapes"]) / len(w["shapes"])
-        per_n[str(N)] = {"us_per_launch": us, "GB/s": nbytes / (us * 1e-6) / 1e9,
-                         "tflops_dense_equiv": fl / (us * 1e-6) / 1e12}
-    line["kernels"]["spmm"]["per_N"] = per_n
+                                 "tflops_dense_equiv": flops / (r["spmm_ms"] / args.steps * 1e-3) / 1e12,
+                                 "tensor_peak_tflops": tpeak, "tensor_peak_source": tpeak_src,
+                                 "groups": per_group}}}
     if r.get("extra_prune"):
         line["kernels"]["prune_compress_bf16"] = r["extra_prune"]
     if rank == 0 and not args.no_e2e:

@@ -85,6 +85,18 @@ typedef enum st24_kernel {
     ST24_KERNEL_MMA_SP = 2    /* warp-level mma.sp (all input types) */
 } st24_kernel;
 
+/* Option bits for st24_spmm_ex (OR them together; 0 = none). */
+typedef enum st24_spmm_flags {
+    /* A_values and A_meta are fixed weights: no work that may still be running
+       on `stream` when the call is enqueued writes them (they were written by
+       work that has completed, or earlier on the stream behind a kernel that
+       does not overlap its successor).  The kernel may then start loading them
+       while the preceding kernel on the stream is still running, which hides
+       the launch-to-launch gap of back-to-back decode-shaped products.  B and C
+       are always read only after the preceding kernel has completed. */
+    ST24_SPMM_FIXED_A = 1
+} st24_spmm_flags;
+
 /* Library version, (major << 16) | (minor << 8) | patch. */
 ST24_API int st24_version(void);
 
@@ -175,13 +187,15 @@ ST24_API st24_status st24_spmm(st24_dtype ab_type, st24_dtype c_type, int64_t M,
                       const float* row_scale, void* workspace, size_t ws_bytes, void* stream);
 
 /*
- * st24_spmm on an explicitly chosen kernel family (for testing one family
- * against another, or a family against the oracle).  ST24_KERNEL_TCGEN05
- * with ab_type ST24_S8 returns ST24_ERR_UNSUPPORTED.  Arguments, workspace
- * and results are as for st24_spmm; st24_spmm_workspace_bytes covers every
- * family.  An unknown `kernel` returns ST24_ERR_INVALID_ARG.
+ * st24_spmm with options: an explicitly chosen kernel family (for testing one
+ * family against another, or a family against the oracle) and `flags`, a set
+ * of st24_spmm_flags bits.  ST24_KERNEL_TCGEN05 with ab_type ST24_S8 returns
+ * ST24_ERR_UNSUPPORTED.  Arguments, workspace and results are as for
+ * st24_spmm (which is st24_spmm_ex with ST24_KERNEL_AUTO and no flags);
+ * st24_spmm_workspace_bytes covers every family.  An unknown `kernel` or an
+ * unknown flag bit returns ST24_ERR_INVALID_ARG.
  */
-ST24_API st24_status st24_spmm_ex(st24_kernel kernel, st24_dtype ab_type, st24_dtype c_type, int64_t M,
+ST24_API st24_status st24_spmm_ex(st24_kernel kernel, unsigned flags, st24_dtype ab_type, st24_dtype c_type, int64_t M,
                                   int64_t N, int64_t K, float alpha, const void* A_values,
                                   const void* A_meta, const void* B, int64_t ldb, float beta, void* C,
                                   int64_t ldc, const float* row_scale, void* workspace, size_t ws_bytes,

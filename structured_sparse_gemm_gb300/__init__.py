@@ -26,6 +26,7 @@ __all__ = [
 
 F16, BF16, E4M3, S8, F32, S32 = 0, 1, 2, 3, 4, 5
 KERNEL_AUTO, KERNEL_TCGEN05, KERNEL_MMA_SP = 0, 1, 2
+SPMM_FIXED_A = 1   # st24_spmm_flags: A is fixed weights no in-flight work on the stream writes
 _KERNELS = {"auto": KERNEL_AUTO, "tcgen05": KERNEL_TCGEN05, "mma_sp": KERNEL_MMA_SP}
 _TORCH_CODE = {
     torch.float16: F16, torch.bfloat16: BF16, torch.float8_e4m3fn: E4M3, torch.int8: S8,
@@ -67,7 +68,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.st24_spmm_workspace_bytes.restype = sz
     lib.st24_spmm.argtypes = [i, i, i64, i64, i64, f, p, p, p, i64, f, p, i64, p, p, sz, p]
     lib.st24_spmm.restype = i
-    lib.st24_spmm_ex.argtypes = [i, i, i, i64, i64, i64, f, p, p, p, i64, f, p, i64, p, p, sz, p]
+    lib.st24_spmm_ex.argtypes = [i, ctypes.c_uint, i, i, i64, i64, i64, f, p, p, p, i64, f, p, i64, p, p, sz, p]
     lib.st24_spmm_ex.restype = i
     lib.st24_spmm_noalloc.argtypes = [i, i, i64, i64, i64, f, p, p, p, i64, f, p, i64, p, p]
     lib.st24_spmm_noalloc.restype = i
@@ -147,11 +148,13 @@ def st24_spmm_workspace_bytes(ab, c, M: int, N: int, K: int) -> int:
 def st24_spmm(values: torch.Tensor, meta: torch.Tensor, X: torch.Tensor, Y: torch.Tensor, *, K: int | None = None,
               alpha: float = 1.0, beta: float = 0.0, row_scale: torch.Tensor | None = None,
               workspace: torch.Tensor | None = None, M: int | None = None, stream=None,
-              kernel: str | int = "auto") -> None:
+              kernel: str | int = "auto", fixed_a: bool = False) -> None:
     """Y[N, M] = alpha * row_scale * (A_sparse @ X.T).T + beta * Y, A given by (values, meta).
 
-    ``kernel`` picks the kernel family ("auto", "tcgen05" or "mma_sp"); anything
-    but "auto" goes through st24_spmm_ex."""
+    ``kernel`` picks the kernel family ("auto", "tcgen05" or "mma_sp");
+    ``fixed_a`` declares (values, meta) fixed weights that no work still in
+    flight on the stream writes (ST24_SPMM_FIXED_A).  Anything but the
+    defaults goes through st24_spmm_ex."""
     N, Kx = X.shape
     K = Kx if K is None else K
     M = Y.shape[1] if M is None else M
@@ -162,10 +165,11 @@ def st24_spmm(values: torch.Tensor, meta: torch.Tensor, X: torch.Tensor, Y: torc
             X.stride(0), float(beta), _ptr(Y), Y.stride(0), _ptr(row_scale), _ptr(workspace), ws_bytes,
             _stream(stream))
     k = _KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
-    if k == KERNEL_AUTO:
+    flags = SPMM_FIXED_A if fixed_a else 0
+    if k == KERNEL_AUTO and flags == 0:
         _check(load().st24_spmm(*args), "st24_spmm")
     else:
-        _check(load().st24_spmm_ex(k, *args), "st24_spmm_ex")
+        _check(load().st24_spmm_ex(k, flags, *args), "st24_spmm_ex")
 
 
 def st24_spmm_noalloc(values: torch.Tensor, meta: torch.Tensor, X: torch.Tensor, Y: torch.Tensor, *,

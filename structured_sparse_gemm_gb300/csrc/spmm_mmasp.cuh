@@ -82,6 +82,7 @@ struct Params : OutParams {
   int64_t K;
   int64_t tiles_m, tiles_n, group_m, k_iters, dp_tiles, sk_tiles;
   int a_evict_first;      // A is read by one output tile only: stream it through L2
+  int a_fixed;            // A is not written by earlier work on the stream: load it before the dependency wait
   int cluster;            // > 1: the CTAs of each split tile form a cluster and reduce in shared memory
   float* partials;       // [2 * gridDim.x][PARTIAL_ELEMS]
   unsigned* counters;    // one per output tile
@@ -162,39 +163,61 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
   }
   __syncthreads();
   // Everything up to grid_dependency_wait overlaps the previous kernel in the
-  // stream.  Inputs are read only after it has completed; the producer first
-  // warms L2 with the weight tiles of its first k-blocks (an L2 prefetch
-  // cannot observe stale data), so they stream from HBM meanwhile.
+  // stream.  Inputs are read only after it has completed -- except, when the
+  // caller declares A fixed (weights no earlier work on the stream writes),
+  // the A and metadata tiles of the first STAGES k-blocks, which the producer
+  // loads into the ring straight away.  Before waiting it also warms L2 with
+  // the weight tiles of the k-blocks after those (an L2 prefetch cannot
+  // observe stale data), so they stream from HBM meanwhile.
   if (threadIdx.x == 0) grid_launch_dependents();
   if (warp != Cfg::CONSUMERS) grid_dependency_wait();
 
   if (warp == Cfg::CONSUMERS) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      {
-        Schedule pre(KI, p.dp_tiles, p.sk_tiles, G, cta);
-        Segment sg;
-        int budget = STAGES;
-        while (budget > 0 && pre.next(sg)) {
-          int64_t mt, nt;
-          tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
-          for (int64_t kb = sg.kb0; kb < sg.kb1 && budget > 0; ++kb, --budget) {
-            tma_prefetch_l2_2d(&tmA, static_cast<int32_t>(kb * (128 / T::ES)), static_cast<int32_t>(mt * Cfg::BM));
-            tma_prefetch_l2_2d(&tmE, static_cast<int32_t>(kb * T::EB), static_cast<int32_t>(mt * Cfg::BM));
-          }
-        }
-      }
-      grid_dependency_wait();
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmE);
       tma_prefetch_desc(&tmB);
       const uint64_t stream_once = p.a_evict_first ? policy_evict_first() : policy_evict_last();
       const uint64_t reuse = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
       uint32_t issued_parity[STAGES];
       bool issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = false;
+      int preloaded = 0;   // leading k-blocks whose A and metadata were loaded before the wait
+      {
+        Schedule pre(KI, p.dp_tiles, p.sk_tiles, G, cta);
+        Segment sg;
+        int warm = 2 * STAGES;   // k-blocks to warm in L2
+        while (warm > 0 && pre.next(sg)) {
+          int64_t mt, nt;
+          tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
+          for (int64_t kb = sg.kb0; kb < sg.kb1 && warm > 0; ++kb) {
+            const int32_t ka = static_cast<int32_t>(kb * (128 / T::ES));
+            const int32_t ke = static_cast<int32_t>(kb * T::EB);
+            const int32_t m0 = static_cast<int32_t>(mt * Cfg::BM);
+            if (p.a_fixed && preloaded < STAGES) {
+              // The ring starts empty: stage `preloaded` is free.  Its full
+              // barrier expects the whole stage; B follows after the wait.
+              const uint32_t fb = smem_u32(&full_bar[preloaded]);
+              uint8_t* st = smem + preloaded * Cfg::STAGE_BYTES;
+              mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
+              tma_load_2d(smem_u32(st), &tmA, ka, m0, fb, stream_once);
+              tma_load_2d(smem_u32(st + Cfg::A_BYTES + Cfg::B_BYTES), &tmE, ke, m0, fb, stream_once);
+              issued[preloaded] = true;
+              issued_parity[preloaded] = 0;
+              ++preloaded;
+            } else {
+              tma_prefetch_l2_2d(&tmA, ka, m0);
+              tma_prefetch_l2_2d(&tmE, ke, m0);
+              --warm;
+            }
+          }
+        }
+      }
+      grid_dependency_wait();
+      int stage = 0;
+      uint32_t phase = 0;
+      int done = 0;   // k-blocks issued so far
       bool ok = true;
       Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, cta);
       Segment sg;
@@ -203,20 +226,22 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
         int64_t mt64, nt64;
         tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mt64, nt64);
         const int32_t mt = static_cast<int32_t>(mt64), nt = static_cast<int32_t>(nt64);
-        for (int64_t kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) { ok = false; break; }
+        for (int64_t kb = kb0; kb < kb1; ++kb, ++done) {
           const uint32_t fb = smem_u32(&full_bar[stage]);
-          mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
           uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
-          const int32_t ka = static_cast<int32_t>(kb * (128 / T::ES));   // compressed A column
           const int32_t kB = static_cast<int32_t>(kb * T::BK);           // logical K
-          tma_load_2d(smem_u32(st), &tmA, ka, mt * Cfg::BM, fb, stream_once);
+          if (done >= preloaded) {
+            if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) { ok = false; break; }
+            mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
+            const int32_t ka = static_cast<int32_t>(kb * (128 / T::ES));   // compressed A column
+            tma_load_2d(smem_u32(st), &tmA, ka, mt * Cfg::BM, fb, stream_once);
+            tma_load_2d(smem_u32(st + Cfg::A_BYTES + Cfg::B_BYTES), &tmE,
+                        static_cast<int32_t>(kb * T::EB), mt * Cfg::BM, fb, stream_once);
+            issued[stage] = true;
+            issued_parity[stage] = phase;
+          }
           tma_load_2d(smem_u32(st + Cfg::A_BYTES), &tmB, kB, nt * BN, fb, reuse);
           tma_load_2d(smem_u32(st + Cfg::A_BYTES + BN * 128), &tmB, kB + 128 / T::ES, nt * BN, fb, reuse);
-          tma_load_2d(smem_u32(st + Cfg::A_BYTES + Cfg::B_BYTES), &tmE,
-                      static_cast<int32_t>(kb * T::EB), mt * Cfg::BM, fb, stream_once);
-          issued[stage] = true;
-          issued_parity[stage] = phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -489,6 +514,7 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
   p.dp_tiles = plan.dp_tiles;
   p.sk_tiles = plan.sk_tiles;
   p.a_evict_first = plan.tiles_n == 1 ? 1 : 0;
+  p.a_fixed = (a.flags & ST24_SPMM_FIXED_A) ? 1 : 0;
   p.cluster = plan.cluster;
   p.alpha = a.alpha; p.beta = a.beta;
   p.C = a.C; p.ldc = a.ldc; p.c_type = a.c;

@@ -84,8 +84,10 @@ struct TcConfig {
 
 struct TcParams : OutParams {
   int64_t K;
+  int prefetch_c;          // beta != 0 and C has a tensor map: warm L2 with each tile's C early
   int64_t tiles_m, tiles_n, group_m, k_iters, dp_tiles, sk_tiles;
   int a_evict_first;      // A is read by one output tile only: stream it through L2
+  int a_fixed;            // A is not written by earlier work on the stream: load it before the dependency wait
   float* partials;
   unsigned* counters;
   unsigned* status;
@@ -94,7 +96,8 @@ struct TcParams : OutParams {
 template <int DT, int BN, int STAGES>
 __global__ void __launch_bounds__(320, 1)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmE,
-                   const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
+                   const TcParams p) {
   using Cfg = TcConfig<DT, BN, STAGES>;
   using T = TcTraits<DT>;
 
@@ -135,39 +138,65 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // Everything up to grid_dependency_wait overlaps the previous kernel in the
-  // stream.  Inputs are read only after it has completed; the producer first
-  // warms L2 with the weight tiles of its first k-blocks (an L2 prefetch
-  // cannot observe stale data), so they stream from HBM meanwhile.
+  // stream.  Inputs are read only after it has completed -- except, when the
+  // caller declares A fixed (weights no earlier work on the stream writes),
+  // the A and metadata tiles of the first STAGES k-blocks, which the producer
+  // loads into the ring straight away.  Before waiting it also warms L2 with
+  // the weight tiles of the k-blocks after those (an L2 prefetch cannot
+  // observe stale data), so they stream from HBM meanwhile.
   if (threadIdx.x == 0) grid_launch_dependents();
   if (warp != 0) grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      {
-        Schedule pre(KI, p.dp_tiles, p.sk_tiles, G, cta);
-        Segment sg;
-        int budget = STAGES;
-        while (budget > 0 && pre.next(sg)) {
-          int64_t mt, nt;
-          tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
-          for (int64_t kb = sg.kb0; kb < sg.kb1 && budget > 0; ++kb, --budget) {
-            tma_prefetch_l2_2d(&tmA, static_cast<int32_t>(kb * (128 / T::ES)), static_cast<int32_t>(mt * Cfg::BM));
-            tma_prefetch_l2_2d(&tmE, static_cast<int32_t>(kb * T::EB), static_cast<int32_t>(mt * Cfg::BM));
-          }
-        }
-      }
-      grid_dependency_wait();
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmE);
       tma_prefetch_desc(&tmB);
       const uint64_t stream_once = p.a_evict_first ? policy_evict_first() : policy_evict_last();
       const uint64_t reuse = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
       uint32_t issued_parity[STAGES];
       bool issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = false;
+      // A and metadata of k-block kb of m-tile mt into stage st (full barrier fb).
+      auto load_weights = [&](uint8_t* st, uint32_t fb, int64_t kb, int32_t m0) {
+        tma_load_2d(smem_u32(st), &tmA, static_cast<int32_t>(kb * (128 / T::ES)), m0, fb, stream_once);
+        uint8_t* se = st + Cfg::A_BYTES + Cfg::B_BYTES;
+        const int32_t ke = static_cast<int32_t>(kb * T::EB);
+        tma_load_2d(smem_u32(se), &tmE, ke, m0, fb, stream_once);
+        if constexpr (T::EB == 32) tma_load_2d(smem_u32(se + 2048), &tmE, ke + 16, m0, fb, stream_once);
+      };
+      int preloaded = 0;   // leading k-blocks whose A and metadata were loaded before the wait
+      {
+        Schedule pre(KI, p.dp_tiles, p.sk_tiles, G, cta);
+        Segment sg;
+        int warm = 2 * STAGES;   // k-blocks to warm in L2
+        while (warm > 0 && pre.next(sg)) {
+          int64_t mt, nt;
+          tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
+          const int32_t m0 = static_cast<int32_t>(mt * Cfg::BM);
+          for (int64_t kb = sg.kb0; kb < sg.kb1 && warm > 0; ++kb) {
+            if (p.a_fixed && preloaded < STAGES) {
+              // The ring starts empty: stage `preloaded` is free.  Its full
+              // barrier expects the whole stage; B follows after the wait.
+              const uint32_t fb = smem_u32(&full_bar[preloaded]);
+              mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
+              load_weights(smem + preloaded * Cfg::STAGE_BYTES, fb, kb, m0);
+              issued[preloaded] = true;
+              issued_parity[preloaded] = 0;
+              ++preloaded;
+            } else {
+              tma_prefetch_l2_2d(&tmA, static_cast<int32_t>(kb * (128 / T::ES)), m0);
+              tma_prefetch_l2_2d(&tmE, static_cast<int32_t>(kb * T::EB), m0);
+              --warm;
+            }
+          }
+        }
+      }
+      grid_dependency_wait();
+      int stage = 0;
+      uint32_t phase = 0;
+      int done = 0;   // k-blocks issued so far
       bool ok = true;
       Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, cta);
       Segment sg;
@@ -176,22 +205,21 @@ __global__ void __launch_bounds__(320, 1)
         int64_t mt64, nt64;
         tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mt64, nt64);
         const int32_t mt = static_cast<int32_t>(mt64), nt = static_cast<int32_t>(nt64);
-        for (int64_t kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) { ok = false; break; }
+        // The epilogue of this tile reads C (beta != 0): start it towards L2 now.
+        if (p.prefetch_c && kb1 == KI) tma_prefetch_l2_2d(&tmC, mt * Cfg::BM, nt * BN);
+        for (int64_t kb = kb0; kb < kb1; ++kb, ++done) {
           const uint32_t fb = smem_u32(&full_bar[stage]);
-          mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
           uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
-          const int32_t ka = static_cast<int32_t>(kb * (128 / T::ES));
+          if (done >= preloaded) {
+            if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) { ok = false; break; }
+            mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
+            load_weights(st, fb, kb, mt * Cfg::BM);
+            issued[stage] = true;
+            issued_parity[stage] = phase;
+          }
           const int32_t kB = static_cast<int32_t>(kb * T::BK);
-          tma_load_2d(smem_u32(st), &tmA, ka, mt * Cfg::BM, fb, stream_once);
           tma_load_2d(smem_u32(st + Cfg::A_BYTES), &tmB, kB, nt * BN, fb, reuse);
           tma_load_2d(smem_u32(st + Cfg::A_BYTES + BN * 128), &tmB, kB + 128 / T::ES, nt * BN, fb, reuse);
-          uint8_t* se = st + Cfg::A_BYTES + Cfg::B_BYTES;
-          const int32_t ke = static_cast<int32_t>(kb * T::EB);
-          tma_load_2d(smem_u32(se), &tmE, ke, mt * Cfg::BM, fb, stream_once);
-          if constexpr (T::EB == 32) tma_load_2d(smem_u32(se + 2048), &tmE, ke + 16, mt * Cfg::BM, fb, stream_once);
-          issued[stage] = true;
-          issued_parity[stage] = phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -420,7 +448,20 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
                             CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !encode_tensor_map_2d(&tmB, ty, a.B, a.K, a.N, a.ldb * T::ES, 128 / T::ES, BN, CU_TENSOR_MAP_SWIZZLE_128B))
     return ST24_ERR_CUDA;
+  // C (element (m, n) at C[n*ldc + m]) as an M-inner 2-D tensor, for the L2
+  // prefetch of each tile's C block when beta != 0.
+  CUtensorMap tmC;
+  bool have_c = false;
+  if (a.beta != 0.0f) {
+    const int cs = elem_size(a.c);
+    const CUtensorMapDataType cty = cs == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    have_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && ((a.ldc * cs) % 16 == 0) &&
+             encode_tensor_map_2d(&tmC, cty, a.C, a.M, a.N, a.ldc * cs, Cfg::BM, BN,
+                                  CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  if (!have_c) tmC = tmA;   // unused
   TcParams p{};
+  p.prefetch_c = have_c ? 1 : 0;
   p.M = a.M; p.N = a.N; p.K = a.K;
   p.alpha = a.alpha; p.beta = a.beta;
   p.C = a.C; p.ldc = a.ldc; p.c_type = a.c;
@@ -432,6 +473,7 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
   p.dp_tiles = plan.dp_tiles;
   p.sk_tiles = plan.sk_tiles;
   p.a_evict_first = plan.tiles_n == 1 ? 1 : 0;
+  p.a_fixed = (a.flags & ST24_SPMM_FIXED_A) ? 1 : 0;
   p.partials = static_cast<float*>(a.workspace);
   p.counters = plan.ws_bytes ? reinterpret_cast<unsigned*>(static_cast<uint8_t*>(a.workspace) +
                                                           2 * static_cast<size_t>(plan.grid) * plan.partial_bytes)
@@ -455,7 +497,7 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmA, tmE, tmB, p) == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmE, tmB, tmC, p) == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;
 }
 
 template <int DT>

@@ -253,13 +253,15 @@ size_t st24_spmm_workspace_bytes(st24_dtype ab_type, st24_dtype c_type, int64_t 
   return ws;
 }
 
-st24_status st24_spmm_ex(st24_kernel kernel, st24_dtype ab_type, st24_dtype c_type, int64_t M, int64_t N,
-                         int64_t K, float alpha, const void* A_values, const void* A_meta, const void* B,
+st24_status st24_spmm_ex(st24_kernel kernel, unsigned flags, st24_dtype ab_type, st24_dtype c_type, int64_t M,
+                         int64_t N, int64_t K, float alpha, const void* A_values, const void* A_meta, const void* B,
                          int64_t ldb, float beta, void* C, int64_t ldc, const float* row_scale,
                          void* workspace, size_t ws_bytes, void* stream) {
   if (kernel != ST24_KERNEL_AUTO && kernel != ST24_KERNEL_TCGEN05 && kernel != ST24_KERNEL_MMA_SP)
     return ST24_ERR_INVALID_ARG;
+  if (flags & ~static_cast<unsigned>(ST24_SPMM_FIXED_A)) return ST24_ERR_INVALID_ARG;
   SpmmArgs a{};
+  a.flags = flags;
   a.ab = ab_type;
   a.c = c_type;
   a.M = M;
@@ -294,7 +296,7 @@ st24_status st24_spmm(st24_dtype ab_type, st24_dtype c_type, int64_t M, int64_t 
                       float alpha, const void* A_values, const void* A_meta, const void* B,
                       int64_t ldb, float beta, void* C, int64_t ldc, const float* row_scale,
                       void* workspace, size_t ws_bytes, void* stream) {
-  return st24_spmm_ex(ST24_KERNEL_AUTO, ab_type, c_type, M, N, K, alpha, A_values, A_meta, B, ldb, beta, C, ldc,
+  return st24_spmm_ex(ST24_KERNEL_AUTO, 0u, ab_type, c_type, M, N, K, alpha, A_values, A_meta, B, ldb, beta, C, ldc,
                       row_scale, workspace, ws_bytes, stream);
 }
 

@@ -58,6 +58,7 @@ struct SpmmArgs {
   const float* row_scale;
   void* workspace;
   size_t ws_bytes;
+  unsigned flags;          // st24_spmm_flags
 };
 
 // A split of the output into BM x BN tiles and of each tile's K loop into

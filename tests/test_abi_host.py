@@ -96,3 +96,14 @@ def test_spmm_rejects_bad_arguments(lib):
     assert call(ldb=260) == 3                            # ldb * 2 bytes not a multiple of 16
     assert call(C=FAKE + 1) == 3                         # C not aligned to its element
     assert call(M=0, v=None, e=None, B=None, C=None) == 0    # empty: no-op
+
+
+def test_spmm_ex_rejects_unknown_kernel_and_flags(lib):
+    def call(kernel=0, flags=0):
+        return lib.st24_spmm_ex(kernel, flags, st.BF16, st.BF16, 128, 8, 256, 1.0, FAKE, FAKE, FAKE, 256, 0.0,
+                                FAKE, 128, None, None, 0, None)
+
+    assert call(kernel=3) == 1
+    assert call(flags=2) == 1
+    assert call(flags=1 << 31) == 1
+    assert call(kernel=7, flags=1) == 1

@@ -148,6 +148,34 @@ def test_decode_bf16_full(kernel, N):
     check_full(inputs.decode_bf16(N), kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("N", [1, 32, 200])
+def test_fixed_weights_back_to_back(kernel, N):
+    """Products over several weights enqueued back to back with ST24_SPMM_FIXED_A
+    (weight tiles loaded while the previous product still runs) equal the same
+    products without it, bit for bit, and the first one matches the oracle."""
+    cases = [inputs.spmm_case("bf16", "bf16", 1024, N, 2048, seed=40 + i) for i in range(4)]
+    layers = []
+    for c in cases:
+        values, meta = st.compress(c.A.to(DEV))
+        layers.append((values, meta, c.X.to(DEV)))
+    torch.cuda.synchronize()
+    wsz = st.st24_spmm_workspace_bytes("bf16", "bf16", 1024, N, 2048)
+    ws = torch.zeros(max(wsz, 1), dtype=torch.uint8, device=DEV)   # one workspace shared by the chain
+    outs = {}
+    for fixed in (False, True):
+        Ys = [torch.empty((N, 1024), dtype=torch.bfloat16, device=DEV) for _ in layers]
+        for _ in range(2):
+            for (values, meta, X), Y in zip(layers, Ys):
+                st.st24_spmm(values, meta, X, Y, K=2048, workspace=ws, kernel=kernel, fixed_a=fixed)
+        torch.cuda.synchronize()
+        outs[fixed] = Ys
+    assert st.st24_device_status() == 0
+    for a, b in zip(outs[False], outs[True]):
+        assert torch.equal(a, b)
+    assert_close(decode_out(outs[True][0]), oracle_full(cases[0]), "bf16", "bf16", "fixed weights")
+
+
 def test_kernel_families_agree():
     # the two kernel families compute the same sums; on one k-block per tile they agree closely
     case = inputs.spmm_case("bf16", "f32", 512, 96, 2048, seed=5)
