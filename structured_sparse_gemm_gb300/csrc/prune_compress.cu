@@ -108,6 +108,116 @@ __device__ __forceinline__ uint2 compress_piece(const uint4 in, uint32_t& meta_b
   return make_uint2(out[0], out[1]);
 }
 
+// ---- the same selection on several groups at once ("SIMD within a register")
+// Lanes of a 32-bit word hold one group each (16-bit lanes: 2 groups, 8-bit
+// lanes: 4 groups).  With every magnitude key below its lane's top bit,
+// (k_i | TOP) - k_j has the lane's top bit set exactly when k_i >= k_j and
+// never borrows from the next lane, so one subtraction compares all lanes.
+// The keep rule is the majority formulation of compress_group, evaluated on
+// the lanes' top bits; a byte permute that replicates each lane's top bit
+// turns the result into lane masks for the selects.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+template <int LANE>
+struct Lanes {
+  static constexpr uint32_t TOP = LANE == 16 ? 0x80008000u : 0x80808080u;
+  static constexpr uint32_t ONE = LANE == 16 ? 0x00010001u : 0x01010101u;
+  // prmt selector: every byte takes the sign (top bit) of its lane's top byte.
+  static constexpr uint32_t SPREAD = LANE == 16 ? 0xBB99u : 0xBA98u;
+};
+
+__device__ __forceinline__ uint32_t maj(uint32_t a, uint32_t b, uint32_t c) { return (a & b) | (a & c) | (b & c); }
+
+// k[i]: keys of element i of every lane's group; x[i]: the raw elements.
+// v0, v1: the kept pair of every lane (lower index first); nib: its nibble
+// i0 | i1 << 2 in the low bits of every lane.
+template <int LANE>
+__device__ __forceinline__ void select_lanes(const uint32_t (&k)[4], const uint32_t (&x)[4], uint32_t& v0,
+                                             uint32_t& v1, uint32_t& nib) {
+  using L = Lanes<LANE>;
+  const uint32_t T = L::TOP;
+  const uint32_t c01 = ((k[0] | T) - k[1]) & T, c02 = ((k[0] | T) - k[2]) & T, c03 = ((k[0] | T) - k[3]) & T;
+  const uint32_t c12 = ((k[1] | T) - k[2]) & T, c13 = ((k[1] | T) - k[3]) & T, c23 = ((k[2] | T) - k[3]) & T;
+  const uint32_t m0 = prmt(maj(c01, c02, c03), 0, L::SPREAD);
+  const uint32_t m1 = prmt(maj(c01 ^ T, c12, c13), 0, L::SPREAD);
+  const uint32_t m2 = prmt(maj(c02 ^ T, c12 ^ T, c23), 0, L::SPREAD);
+  const uint32_t m3 = prmt(maj(c03 ^ T, c13 ^ T, c23 ^ T), 0, L::SPREAD);
+  v0 = (x[0] & m0) | (~m0 & ((x[1] & m1) | (~m1 & x[2])));
+  v1 = (x[3] & m3) | (~m3 & ((x[2] & m2) | (~m2 & x[1])));
+  const uint32_t one = L::ONE, two = L::ONE << 1;
+  const uint32_t i0 = ~m0 & ((m1 & one) | (~m1 & two));
+  const uint32_t i1 = (m3 & (one | two)) | (~m3 & ((m2 & two) | (~m2 & one)));
+  nib = i0 | (i1 << 2);
+}
+
+// compress_piece on lanes.  Returns false (16-bit types only) when the piece
+// holds a NaN, whose keys need the clamp of mag_key; the caller then uses
+// compress_piece.
+template <int DT, int ES>
+__device__ __forceinline__ bool compress_piece_lanes(const uint4 in, uint2& out, uint32_t& meta_bits) {
+  if constexpr (ES == 2) {
+    // x[i] = element i of group 0 (low lane) and of group 1 (high lane).
+    const uint32_t x[4] = {prmt(in.x, in.z, 0x5410), prmt(in.x, in.z, 0x7632), prmt(in.y, in.w, 0x5410),
+                           prmt(in.y, in.w, 0x7632)};
+    uint32_t k[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) k[i] = x[i] & 0x7FFF7FFFu;
+    // a lane holds a NaN when its key is above the infinity pattern
+    constexpr uint32_t below_top = DT == kBF16 ? 0x007F007Fu : 0x03FF03FFu;
+    if (((k[0] + below_top) | (k[1] + below_top) | (k[2] + below_top) | (k[3] + below_top)) & 0x80008000u)
+      return false;
+    uint32_t v0, v1, nib;
+    select_lanes<16>(k, x, v0, v1, nib);
+    out = make_uint2(prmt(v0, v1, 0x5410), prmt(v0, v1, 0x7632));
+    meta_bits = (nib & 0xFu) | ((nib >> 12) & 0xF0u);
+    return true;
+  } else if constexpr (DT == kE4M3) {
+    // 4x4 byte transpose: x[i] = element i of groups 0..3 (lane g = group g).
+    const uint32_t t0 = prmt(in.x, in.y, 0x5140), t1 = prmt(in.x, in.y, 0x7362);
+    const uint32_t t2 = prmt(in.z, in.w, 0x5140), t3 = prmt(in.z, in.w, 0x7362);
+    const uint32_t x[4] = {prmt(t0, t2, 0x5410), prmt(t0, t2, 0x7632), prmt(t1, t3, 0x5410),
+                           prmt(t1, t3, 0x7632)};
+    // |x| order is the order of the low 7 bits; 0x7F, the only NaN
+    // magnitude, is above every number and ties with itself.
+    uint32_t k[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) k[i] = x[i] & 0x7F7F7F7Fu;
+    uint32_t v0, v1, nib;
+    select_lanes<8>(k, x, v0, v1, nib);
+    out = make_uint2(prmt(v0, v1, 0x5140), prmt(v0, v1, 0x7362));
+    const uint32_t t = nib | (nib >> 4);   // bytes 0 and 2: two nibbles each
+    meta_bits = prmt(t, 0, 0x4420) & 0xFFFFu;
+    return true;
+  } else {
+    // int8: |-128| = 128 needs 8 bits, so 16-bit lanes, two groups per pass;
+    // each element sign-extended into its lane.
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t pairs[2];
+    meta_bits = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t a = w[2 * h], b = w[2 * h + 1];
+      const uint32_t x[4] = {prmt(a, b, 0xC480), prmt(a, b, 0xD591), prmt(a, b, 0xE6A2), prmt(a, b, 0xF7B3)};
+      uint32_t k[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t neg = prmt(x[i], 0, 0xBB99);   // all-ones in negative lanes
+        k[i] = (x[i] ^ neg) + (neg & 0x00010001u);
+      }
+      uint32_t v0, v1, nib;
+      select_lanes<16>(k, x, v0, v1, nib);
+      pairs[h] = prmt(v0, v1, 0x6240);
+      meta_bits |= ((nib & 0xFu) | ((nib >> 12) & 0xF0u)) << (8 * h);
+    }
+    out = make_uint2(pairs[0], pairs[1]);
+    return true;
+  }
+}
+
 template <int ES>
 __device__ __forceinline__ uint4 expand_piece(const uint2 vals, uint32_t meta_bits) {
   uint32_t w[4];
@@ -175,7 +285,8 @@ __global__ void __launch_bounds__(kThreads) prune_compress_vec(
     for (int i = 0; i < kPiecesPerLane; ++i) {
       if (base + i * 32 + lane >= total) break;
       uint32_t mb;
-      const uint2 v = compress_piece<DT, ES>(in[i], mb);
+      uint2 v;
+      if (!compress_piece_lanes<DT, ES>(in[i], v, mb)) v = compress_piece<DT, ES>(in[i], mb);
       const int64_t rr = row[i], cc = col[i];
       *reinterpret_cast<uint2*>(values + rr * v_row_bytes + cc * 8) = v;
       if constexpr (ES == 2)

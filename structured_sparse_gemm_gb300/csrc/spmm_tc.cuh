@@ -343,22 +343,21 @@ __global__ void __launch_bounds__(320, 1)
       const bool row_ok = m < p.M;
       const float f = row_ok ? row_factor(p, m) : 0.0f;
       if (whole) {
+        with_float_c_type(p.c_type, [&](auto ct) {
+          constexpr int CT = decltype(ct)::value;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += CH) {
-          uint32_t r[CH];
-          if constexpr (CH == 32) tmem_ld_x32(tacc + c, r); else tmem_ld_x16(tacc + c, r);
-          tmem_ld_wait();
-          if (row_ok) {
-            float bc[CH];
+          for (int c = 0; c < BN; c += CH) {
+            uint32_t r[CH];
+            if constexpr (CH == 32) tmem_ld_x32(tacc + c, r); else tmem_ld_x16(tacc + c, r);
+            tmem_ld_wait();
+            if (row_ok) {
+              float v[CH];
 #pragma unroll
-            for (int j = 0; j < CH; ++j) bc[j] = (n_base + c + j < p.N) ? load_beta_c(p, m, n_base + c + j) : 0.0f;
-#pragma unroll
-            for (int j = 0; j < CH; ++j) {
-              const int64_t n = n_base + c + j;
-              if (n < p.N) store_out<float>(p, m, n, __uint_as_float(r[j]), f, bc[j]);
+              for (int j = 0; j < CH; ++j) v[j] = __uint_as_float(r[j]);
+              store_row_chunk<CT, CH>(p, m, n_base + c, v, f);
             }
           }
-        }
+        });
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[abuf]));
@@ -414,14 +413,7 @@ __global__ void __launch_bounds__(320, 1)
                 }
               }
             }
-            float bc[RCH];
-#pragma unroll
-            for (int j = 0; j < RCH; ++j) bc[j] = (n_base + c0 + j < p.N) ? load_beta_c(p, m, n_base + c0 + j) : 0.0f;
-#pragma unroll
-            for (int j = 0; j < RCH; ++j) {
-              const int64_t n = n_base + c0 + j;
-              if (n < p.N) store_out<float>(p, m, n, t[j], f, bc[j]);
-            }
+            with_float_c_type(p.c_type, [&](auto ct) { store_row_chunk<decltype(ct)::value, RCH>(p, m, n_base + c0, t, f); });
           }
         }
       }

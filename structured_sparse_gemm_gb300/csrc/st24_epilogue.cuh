@@ -44,6 +44,57 @@ __device__ __forceinline__ float load_beta_c(const OutParams& p, int64_t m, int6
   return p.beta != 0.0f ? __fmul_rn(p.beta, load_c(p, n * p.ldc + m)) : 0.0f;
 }
 
+// The same, with the output type a compile-time constant: no per-element
+// branch on the type, so a chunk's loads issue back to back as predicated
+// instructions and their latencies overlap.
+template <int CT>
+__device__ __forceinline__ float c_load(const void* C, int64_t idx) {
+  if constexpr (CT == kF32) return static_cast<const float*>(C)[idx];
+  else if constexpr (CT == kBF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(C)[idx]);
+  else return __half2float(static_cast<const __half*>(C)[idx]);
+}
+
+template <int CT>
+__device__ __forceinline__ void c_store(void* C, int64_t idx, float r) {
+  if constexpr (CT == kF32) static_cast<float*>(C)[idx] = r;
+  else if constexpr (CT == kBF16) static_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(r);
+  else static_cast<__half*>(C)[idx] = __float2half_rn(r);
+}
+
+// Calls f(std::integral_constant<int, CT>) for the floating-point output
+// type p.c_type (the branch is taken once, outside the caller's loops).
+template <typename F>
+__device__ __forceinline__ void with_float_c_type(int c_type, F&& f) {
+  switch (c_type) {
+    case kF32: f(std::integral_constant<int, kF32>{}); break;
+    case kBF16: f(std::integral_constant<int, kBF16>{}); break;
+    default: f(std::integral_constant<int, kF16>{}); break;
+  }
+}
+
+// Column chunk [n0, n0 + CH) of output row m from fp32 sums v: every beta*C
+// input of the chunk is loaded before any output is stored (the epilogue
+// formula and rounding are those of store_out).
+template <int CT, int CH>
+__device__ __forceinline__ void store_row_chunk(const OutParams& p, int64_t m, int64_t n0, const float (&v)[CH],
+                                                float factor) {
+  float bc[CH];
+  if (p.beta != 0.0f) {
+#pragma unroll
+    for (int j = 0; j < CH; ++j) bc[j] = (n0 + j < p.N) ? c_load<CT>(p.C, (n0 + j) * p.ldc + m) : 0.0f;
+#pragma unroll
+    for (int j = 0; j < CH; ++j) bc[j] = __fmul_rn(p.beta, bc[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < CH; ++j) {
+    if (n0 + j < p.N) {
+      float r = __fmul_rn(v[j], factor);
+      if (p.beta != 0.0f) r = __fadd_rn(r, bc[j]);
+      c_store<CT>(p.C, (n0 + j) * p.ldc + m, r);
+    }
+  }
+}
+
 template <typename Acc>
 __device__ __forceinline__ void store_out(const OutParams& p, int64_t m, int64_t n, Acc acc, float factor,
                                           float beta_c) {
