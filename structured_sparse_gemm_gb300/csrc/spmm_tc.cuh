@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(320, 1)
       Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, cta);
       Segment sg;
       while (ok && sch.next(sg)) {
-        const int64_t tile = sg.tile, kb0 = sg.kb0, kb1 = sg.kb1;
+        const int64_t kb0 = sg.kb0, kb1 = sg.kb1;
         if (!mbar_wait(smem_u32(&tempty_bar[abuf]), aphase ^ 1u, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(abuf * BN);
@@ -347,15 +347,12 @@ __global__ void __launch_bounds__(320, 1)
           constexpr int CT = decltype(ct)::value;
 #pragma unroll 1
           for (int c = 0; c < BN; c += CH) {
+            float bc[CH];
+            if (row_ok && p.beta != 0.0f) load_row_chunk_beta_c<CT, CH>(p, m, n_base + c, bc);
             uint32_t r[CH];
             if constexpr (CH == 32) tmem_ld_x32(tacc + c, r); else tmem_ld_x16(tacc + c, r);
             tmem_ld_wait();
-            if (row_ok) {
-              float v[CH];
-#pragma unroll
-              for (int j = 0; j < CH; ++j) v[j] = __uint_as_float(r[j]);
-              store_row_chunk<CT, CH>(p, m, n_base + c, v, f);
-            }
+            if (row_ok) store_row_chunk_bits<CT, CH>(p, m, n_base + c, r, bc, f);
           }
         });
         tc_fence_before();
@@ -387,35 +384,9 @@ __global__ void __launch_bounds__(320, 1)
           *s_last = last;
         }
         named_barrier_sync(1, 128);
-        if (*s_last && row_ok) {
-          // Sum the partials in k order (segment c_lo first), RCH columns at a
-          // time; up to 4 segments' loads are issued together, so a tile split
-          // over s CTAs costs ceil(s / 4) memory latencies per column chunk.
-          constexpr int RCH = BN < 16 ? BN : 16;
-#pragma unroll 1
-          for (int c0 = 0; c0 < BN; c0 += RCH) {
-            float t[RCH];
-            for (int64_t cb = c_lo; cb <= c_hi; cb += 4) {
-              float v[4][RCH];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                if (cb + u <= c_hi) {
-                  const float* src = p.partials + sch.slot(cb + u, tile) * (Cfg::BM * BN) + 32 * q + lane;
-#pragma unroll
-                  for (int j = 0; j < RCH; ++j) v[u][j] = __ldcg(src + (c0 + j) * Cfg::BM);
-                }
-              }
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                if (cb + u <= c_hi) {
-#pragma unroll
-                  for (int j = 0; j < RCH; ++j) t[j] = (cb + u == c_lo) ? v[u][j] : t[j] + v[u][j];
-                }
-              }
-            }
-            with_float_c_type(p.c_type, [&](auto ct) { store_row_chunk<decltype(ct)::value, RCH>(p, m, n_base + c0, t, f); });
-          }
-        }
+        if (*s_last && row_ok)
+          reduce_split_row<Cfg::BM, BN, (BN < 16 ? BN : 16)>(p, p.partials, sch, tile, 1, 0, c_lo, c_hi,
+                                                             32 * q + lane, m, n_base, f);
       }
       if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
     }
@@ -492,9 +463,21 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmE, tmB, tmC, p) == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;
 }
 
+}  // namespace tc
+}  // namespace st24
+
+#include "spmm_tc2.cuh"
+
+namespace st24 {
+namespace tc {
+
 template <int DT>
 st24_status launch_dt_impl(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev, cudaStream_t s) {
   constexpr bool k16 = TcTraits<DT>::ES == 2;
+  if (plan.pair) {
+    if (plan.bn == 128) return tc2::launch_pair<DT, 128, 5>(a, plan, dev, s);
+    return tc2::launch_pair<DT, 224, 4>(a, plan, dev, s);
+  }
   switch (plan.bn) {
     case 16: return launch_cfg<DT, 16, 8>(a, plan, dev, s);
     case 32: return launch_cfg<DT, 32, 7>(a, plan, dev, s);

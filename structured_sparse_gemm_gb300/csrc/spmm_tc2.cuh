@@ -1,0 +1,504 @@
+// spmm_tc2.cuh -- the tcgen05 sparse-MMA SpMM on CTA pairs, for wide N.
+//
+// Same product and epilogue as spmm_tc.cuh ("Chapter 26 -- Sparsity: The
+// Hardware View", section "2:4 Fine-Grained Structured Sparsity"), with the
+// output tile shared by the two CTAs of a cluster: tcgen05.mma.sp with
+// cta_group::2 computes M = 256 rows (128 rows of A and of the accumulator in
+// each CTA) by N = BNP columns (each CTA stages BNP / 2 rows of B, the MMA
+// reads both halves).  Per CTA this halves the B bytes staged per output
+// element against a one-CTA tile of the same N, which is what bounds the wide
+// products: the pipeline's bytes in flight per SM against L2 latency.
+//
+// Roles (320 threads per CTA, both CTAs):
+//  * warp 0, TMA producer: its CTA's 128 rows of compressed A and metadata and
+//    its BNP / 2 rows of B per stage, on its own full/empty barriers.
+//  * warps 6-9, metadata: shared memory -> this CTA's TMEM (as in the one-CTA
+//    kernel), then signal the leader CTA's meta barrier: the leader's warps
+//    arrive on it (4 arrivals, each expecting 4 bytes), the peer's warps
+//    complete those bytes with an asynchronous 4-byte store into the leader's
+//    shared memory (st.async, whose barrier signal releases at cluster scope
+//    without stalling the warp; a blocking remote arrive cost ~1 us per stage).
+//    Each metadata warp signals only after its own CTA's stage has landed.
+//  * warp 1 of the leader (cluster rank 0), MMA issuer: waits on the meta
+//    barrier, issues the pair MMAs and commits them to the empty barriers and
+//    accumulator barriers of both CTAs (multicast).  Warp 1 of each CTA
+//    allocates and frees TMEM (cta_group::2, both CTAs together).
+//  * warps 2-5, epilogue: this CTA's 128 rows of the accumulator; they arrive
+//    on the leader's accumulator-empty barrier (8 arrivals).  With beta != 0
+//    each warp stages its 32 x 32 chunks of C in shared memory by TMA, one
+//    chunk ahead (double-buffered), instead of 32 scattered loads per chunk.
+// Stream-K over pair tiles: each CTA keeps its own partial tile and counter.
+#pragma once
+
+#include "spmm_tc.cuh"
+
+namespace st24 {
+namespace tc2 {
+
+using tc::TcParams;
+using tc::TcTraits;
+
+template <int DT, int BNP_, int STAGES_>
+struct PairConfig {
+  using T = TcTraits<DT>;
+  static constexpr int BM = 128;                     // rows of A and D per CTA (M = 256 per pair)
+  static constexpr int BNP = BNP_;                   // N of the pair tile
+  static constexpr int BH = BNP / 2;                 // rows of B staged per CTA
+  static constexpr int STAGES = STAGES_;
+  static constexpr int THREADS = 320;
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BH * 256;           // two 128-byte-wide boxes of BH rows
+  static constexpr int E_BYTES = BM * T::EB;
+  static constexpr int STAGE_TX = A_BYTES + B_BYTES + E_BYTES;
+  static constexpr int STAGE_BYTES = (STAGE_TX + 1023) / 1024 * 1024;
+  static constexpr int META_COL0 = 2 * BNP;          // after the two accumulators
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int CBUF_BYTES = 32 * 32 * 4;                     // one warp's 32 x 32 chunk of C (fp32 at most)
+  static constexpr int C_BYTES = 4 * 2 * CBUF_BYTES;                  // 4 epilogue warps, double-buffered
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + C_BYTES + 1024 + 512;   // + alignment, barriers, signal words
+  static constexpr int CH = 32;                      // columns per tcgen05.ld
+  // Instruction descriptor: sparse, fp32 accumulator, K-major A and B, N = BNP, M = 256.
+  static constexpr uint32_t IDESC = (1u << 2) | (1u << 4) | (T::FMT << 7) | (T::FMT << 10) |
+                                    (static_cast<uint32_t>(BNP >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
+  static_assert(BNP % 32 == 0 && BNP >= 64 && BNP <= 256, "N of the pair MMA; B halves of whole swizzle atoms");
+  static_assert(2 * BNP + STAGES * T::META_COLS <= TMEM_COLS, "tensor memory");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  static_assert((3 * STAGES + 5 + 8) * 8 + 8 + STAGES * 16 <= 512, "barrier region");
+};
+
+template <int DT, int BNP, int STAGES>
+__global__ void __launch_bounds__(320, 1)
+    spmm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmE,
+                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
+                    const __grid_constant__ CUtensorMap tmCc, const TcParams p) {
+  using Cfg = PairConfig<DT, BNP, STAGES>;
+  using T = TcTraits<DT>;
+  constexpr uint16_t kBoth = 0x3;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* cbuf = smem + STAGES * Cfg::STAGE_BYTES;   // [4 warps][2][CBUF_BYTES] staged chunks of C
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(cbuf + Cfg::C_BYTES);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* meta_bar = empty_bar + STAGES;      // [STAGES] leader: metadata of both CTAs in TMEM
+  uint64_t* tfull_bar = meta_bar + STAGES;      // [2] accumulator ready
+  uint64_t* tempty_bar = tfull_bar + 2;         // [2] leader: accumulator drained in both CTAs
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint64_t* cbar = drain_bar + 1;               // [4 warps][2] staged C chunk landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cbar + 8);
+  int* s_last = reinterpret_cast<int*>(tmem_slot + 1);
+  uint32_t* meta_sink = reinterpret_cast<uint32_t*>(s_last + 1);   // [STAGES][4] targets of the peer's signals
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();      // 0: the leader, which issues the pair MMAs
+  const int64_t G = gridDim.x / 2, pair = blockIdx.x / 2;
+  const int64_t KI = p.k_iters;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+      mbar_init(smem_u32(&meta_bar[s]), 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull_bar[b]), 1);
+      mbar_init(smem_u32(&tempty_bar[b]), 8);
+    }
+    mbar_init(smem_u32(drain_bar), 1);
+    for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&cbar[i]), 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();   // both CTAs' barriers initialised and TMEM allocated before any cross-CTA use
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // As in the one-CTA kernel: inputs are read after the dependency wait,
+  // except fixed weights (ST24_SPMM_FIXED_A), whose first stages are loaded
+  // before it; L2 is warmed with the weight tiles after those.
+  if (threadIdx.x == 0) grid_launch_dependents();
+  if (warp != 0) grid_dependency_wait();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmE);
+      tma_prefetch_desc(&tmB);
+      const uint64_t stream_once = p.a_evict_first ? policy_evict_first() : policy_evict_last();
+      const uint64_t reuse = policy_evict_last();
+      uint32_t issued_parity[STAGES];
+      bool issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = false;
+      auto load_weights = [&](uint8_t* st, uint32_t fb, int64_t kb, int32_t m0) {
+        tma_load_2d(smem_u32(st), &tmA, static_cast<int32_t>(kb * (128 / T::ES)), m0, fb, stream_once);
+        uint8_t* se = st + Cfg::A_BYTES + Cfg::B_BYTES;
+        const int32_t ke = static_cast<int32_t>(kb * T::EB);
+        tma_load_2d(smem_u32(se), &tmE, ke, m0, fb, stream_once);
+        if constexpr (T::EB == 32) tma_load_2d(smem_u32(se + 2048), &tmE, ke + 16, m0, fb, stream_once);
+      };
+      int preloaded = 0;
+      {
+        Schedule pre(KI, p.dp_tiles, p.sk_tiles, G, pair);
+        Segment sg;
+        int warm = 2 * STAGES;
+        while (warm > 0 && pre.next(sg)) {
+          int64_t mt, nt;
+          tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
+          const int32_t m0 = static_cast<int32_t>((2 * mt + rank) * Cfg::BM);
+          for (int64_t kb = sg.kb0; kb < sg.kb1 && warm > 0; ++kb) {
+            if (p.a_fixed && preloaded < STAGES) {
+              const uint32_t fb = smem_u32(&full_bar[preloaded]);
+              mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
+              load_weights(smem + preloaded * Cfg::STAGE_BYTES, fb, kb, m0);
+              issued[preloaded] = true;
+              issued_parity[preloaded] = 0;
+              ++preloaded;
+            } else {
+              tma_prefetch_l2_2d(&tmA, static_cast<int32_t>(kb * (128 / T::ES)), m0);
+              tma_prefetch_l2_2d(&tmE, static_cast<int32_t>(kb * T::EB), m0);
+              --warm;
+            }
+          }
+        }
+      }
+      grid_dependency_wait();
+      int stage = 0;
+      uint32_t phase = 0;
+      int done = 0;
+      bool ok = true;
+      Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, pair);
+      Segment sg;
+      while (ok && sch.next(sg)) {
+        int64_t mt64, nt64;
+        tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt64, nt64);
+        const int32_t m0 = static_cast<int32_t>((2 * mt64 + rank) * Cfg::BM);
+        const int32_t n0 = static_cast<int32_t>(nt64 * BNP + rank * Cfg::BH);
+        if (p.prefetch_c && sg.kb1 == KI) tma_prefetch_l2_2d(&tmC, m0, static_cast<int32_t>(nt64 * BNP));
+        for (int64_t kb = sg.kb0; kb < sg.kb1; ++kb, ++done) {
+          const uint32_t fb = smem_u32(&full_bar[stage]);
+          uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
+          if (done >= preloaded) {
+            if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) { ok = false; break; }
+            mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
+            load_weights(st, fb, kb, m0);
+            issued[stage] = true;
+            issued_parity[stage] = phase;
+          }
+          const int32_t kB = static_cast<int32_t>(kb * T::BK);
+          tma_load_2d(smem_u32(st + Cfg::A_BYTES), &tmB, kB, n0, fb, reuse);
+          tma_load_2d(smem_u32(st + Cfg::A_BYTES + Cfg::BH * 128), &tmB, kB + 128 / T::ES, n0, fb, reuse);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      for (int s = 0; s < STAGES; ++s)
+        if (issued[s]) mbar_wait(smem_u32(&full_bar[s]), issued_parity[s], p.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int abuf = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, pair);
+      Segment sg;
+      while (ok && sch.next(sg)) {
+        if (!mbar_wait_cluster(smem_u32(&tempty_bar[abuf]), aphase ^ 1u, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(abuf * BNP);
+        for (int64_t kb = sg.kb0; kb < sg.kb1; ++kb) {
+          // Both CTAs' metadata warps arrive only after their own stage landed.
+          if (!mbar_wait_cluster(smem_u32(&meta_bar[stage]), phase, p.status)) { ok = false; break; }
+          tc_fence_after();
+          uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
+          const uint32_t mcol = tmem + static_cast<uint32_t>(Cfg::META_COL0 + stage * T::META_COLS);
+          const int64_t ks_left = (p.K - kb * T::BK) / T::KSTEP;
+          const int ksteps = ks_left < 4 ? static_cast<int>(ks_left) : 4;
+          const uint32_t a0 = smem_u32(st), b0 = smem_u32(st + Cfg::A_BYTES);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            if (ks >= ksteps) break;
+            const uint64_t da = smem_desc(a0 + ks * 32, 16, 1024, kSwizzle128B);
+            const uint64_t db = smem_desc(b0 + (ks >> 1) * (Cfg::BH * 128) + (ks & 1) * 64, 16, 1024, kSwizzle128B);
+            const uint32_t acc = (kb > sg.kb0 || ks > 0) ? 1u : 0u;
+            if constexpr (T::ES == 2)
+              tc_mma_sp_f16_pair(d, da, db, mcol + 4 * ks, Cfg::IDESC, acc);
+            else
+              tc_mma_sp_f8f6f4_pair(d, da, db, mcol + 4 * ks, Cfg::IDESC, acc);
+          }
+          tc_commit_pair(smem_u32(&empty_bar[stage]), kBoth);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit_pair(smem_u32(&tfull_bar[abuf]), kBoth);
+        if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
+      }
+      // Both CTAs learn when every pair MMA has completed (before TMEM is freed).
+      tc_commit_pair(smem_u32(drain_bar), kBoth);
+      mbar_wait(smem_u32(drain_bar), 0, p.status);
+    } else if (lane == 0) {
+      mbar_wait(smem_u32(drain_bar), 0, p.status);
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ metadata
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    const uint4 fill = make_uint4(0x44444444u, 0x44444444u, 0x44444444u, 0x44444444u);  // index pair (0, 1)
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, pair);
+    Segment sg;
+    while (ok && sch.next(sg)) {
+      int64_t mt, nt;
+      tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
+      const int64_t rows_valid = p.M - (2 * mt + rank) * Cfg::BM;   // rows past M hold zero-filled metadata
+      for (int64_t kb = sg.kb0; kb < sg.kb1; ++kb) {
+        if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.status)) { ok = false; break; }
+        const uint8_t* se = smem + stage * Cfg::STAGE_BYTES + Cfg::A_BYTES + Cfg::B_BYTES;
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) +
+                               static_cast<uint32_t>(Cfg::META_COL0 + stage * T::META_COLS);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = fill.x;
+        if constexpr (T::ES == 2) {
+          const int j = row & 15;
+          const int partner = j < 8 ? row + 8 : row - 8;
+          const uint4 own = row < rows_valid ? *reinterpret_cast<const uint4*>(se + row * 16) : fill;
+          const uint4 oth = partner < rows_valid ? *reinterpret_cast<const uint4*>(se + partner * 16) : fill;
+          const uint4 lo = j < 8 ? own : oth, hi = j < 8 ? oth : own;
+          const uint32_t sel = j < 8 ? 0x5410u : 0x7632u;
+          w[0] = __byte_perm(lo.x, hi.x, sel);
+          w[4] = __byte_perm(lo.y, hi.y, sel);
+          w[8] = __byte_perm(lo.z, hi.z, sel);
+          w[12] = __byte_perm(lo.w, hi.w, sel);
+        } else {
+          const bool in = row < rows_valid;
+          const uint4 a = in ? *reinterpret_cast<const uint4*>(se + row * 16) : fill;
+          const uint4 b = in ? *reinterpret_cast<const uint4*>(se + 2048 + row * 16) : fill;
+          w[0] = a.x; w[1] = a.y; w[4] = a.z; w[5] = a.w;
+          w[8] = b.x; w[9] = b.y; w[12] = b.z; w[13] = b.w;
+        }
+        tmem_st_x16(taddr, w);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0)
+            mbar_arrive_expect_tx(smem_u32(&meta_bar[stage]), 4);
+          else
+            signal_tx_cluster(smem_u32(&meta_sink[stage * 4 + q]), smem_u32(&meta_bar[stage]), 0);
+        }
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    int abuf = 0;
+    uint32_t aphase = 0;
+    constexpr int CH = Cfg::CH;
+    // beta * C from staged chunks when C has a tensor map (else scattered loads).
+    const bool stage_c = p.beta != 0.0f && p.prefetch_c;
+    uint8_t* my_cbuf = cbuf + q * 2 * Cfg::CBUF_BYTES;
+    uint64_t* my_cbar = cbar + 2 * q;
+    uint32_t cpar[2] = {0u, 0u};
+    const uint64_t c_once = policy_evict_first();
+    Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, pair);
+    Segment sg;
+    while (sch.next(sg)) {
+      const int64_t tile = sg.tile, kb0 = sg.kb0, kb1 = sg.kb1;
+      int64_t mt, nt;
+      tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
+      const int64_t m = (2 * mt + rank) * Cfg::BM + 32 * q + lane;
+      const int64_t n_base = nt * BNP;
+      if (!mbar_wait(smem_u32(&tfull_bar[abuf]), aphase, p.status)) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(abuf * BNP);
+      const bool whole = (kb0 == 0 && kb1 == KI);
+      const bool row_ok = m < p.M;
+      const float f = row_ok ? row_factor(p, m) : 0.0f;
+      if (whole) {
+        with_float_c_type(p.c_type, [&](auto ct) {
+          constexpr int CT = decltype(ct)::value;
+          constexpr uint32_t CS = CT == kF32 ? 4u : 2u;
+          const int32_t cm = static_cast<int32_t>((2 * mt + rank) * Cfg::BM + 32 * q);   // this warp's 32 rows
+          // Chunk c of C (32 rows x 32 columns) into buffer (c / CH) & 1 of this warp.
+          auto stage_chunk = [&](int c) {
+            const int b = (c / CH) & 1;
+            fence_proxy_async_smem();   // this buffer's earlier reads come before the copy's writes
+            mbar_arrive_expect_tx(smem_u32(&my_cbar[b]), 32u * 32u * CS);
+            tma_load_2d(smem_u32(my_cbuf + b * Cfg::CBUF_BYTES), &tmCc, cm, static_cast<int32_t>(n_base + c),
+                        smem_u32(&my_cbar[b]), c_once);
+          };
+          if (stage_c && lane == 0) stage_chunk(0);
+#pragma unroll 1
+          for (int c = 0; c < BNP; c += CH) {
+            const bool in_n = n_base + c < p.N;
+            const bool live = row_ok && in_n;
+            if (stage_c && lane == 0 && c + CH < BNP && n_base + c + CH < p.N) stage_chunk(c + CH);
+            uint32_t r[CH];
+            tmem_ld_x32(tacc + c, r);
+            tmem_ld_wait();
+            float bc[CH];
+            if (stage_c && in_n) {
+              const int b = (c / CH) & 1;
+              mbar_wait(smem_u32(&my_cbar[b]), cpar[b], p.status);
+              cpar[b] ^= 1u;
+              staged_beta_c<CT, CH>(smem_u32(my_cbuf + b * Cfg::CBUF_BYTES), lane, p.beta, bc);
+              __syncwarp();   // every lane has read this buffer before it is staged again
+            } else if (live && p.beta != 0.0f) {
+              load_row_chunk_beta_c<CT, CH>(p, m, n_base + c, bc);
+            }
+            if (live) store_row_chunk_bits<CT, CH>(p, m, n_base + c, r, bc, f);
+          }
+        });
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(smem_u32(&tempty_bar[abuf]), 0);
+      } else {
+        // This CTA's half of the pair tile: slot 2 * (pair slot) + rank.
+        float* mine = p.partials + (2 * sch.slot(pair, tile) + rank) * (Cfg::BM * BNP);
+#pragma unroll 1
+        for (int c = 0; c < BNP; c += CH) {
+          uint32_t r[CH];
+          tmem_ld_x32(tacc + c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < CH; ++j) __stcg(mine + (c + j) * Cfg::BM + 32 * q + lane, __uint_as_float(r[j]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(smem_u32(&tempty_bar[abuf]), 0);
+        __threadfence();
+        named_barrier_sync(1, 128);
+        const int64_t c_lo = sch.first_cta(tile);
+        const int64_t c_hi = sch.last_cta(tile);
+        if (threadIdx.x == 64) {
+          unsigned* counter = p.counters + 2 * tile + rank;
+          const unsigned nseg = static_cast<unsigned>(c_hi - c_lo + 1);
+          const unsigned old = atomicAdd(counter, 1u);
+          const int last = (old == nseg - 1) ? 1 : 0;
+          if (last) *counter = 0;   // all contributors have arrived: ready for the next call
+          __threadfence();
+          *s_last = last;
+        }
+        named_barrier_sync(1, 128);
+        if (*s_last && row_ok)
+          reduce_split_row<Cfg::BM, BNP, 16>(p, p.partials, sch, tile, 2, static_cast<int>(rank), c_lo, c_hi,
+                                             32 * q + lane, m, n_base, f);
+      }
+      if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, Cfg::TMEM_COLS);
+  // Neither CTA leaves while the other may still arrive on its barriers.
+  cluster_sync();
+}
+
+// Pairs that can be resident at once for this kernel (its clusters of 2).
+template <int DT, int BNP, int STAGES>
+int resident_pairs(int num_sms) {
+  using Cfg = PairConfig<DT, BNP, STAGES>;
+  static int pairs = 0;
+  if (pairs == 0) {
+    auto kern = spmm_tc2_kernel<DT, BNP, STAGES>;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(num_sms / 2 * 2));
+      cfg.blockDim = dim3(Cfg::THREADS);
+      cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = 2;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    }
+    pairs = n > 0 ? (n < num_sms / 2 ? n : num_sms / 2) : num_sms / 2;
+  }
+  return pairs;
+}
+
+template <int DT, int BNP, int STAGES>
+st24_status launch_pair(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev, cudaStream_t stream) {
+  using Cfg = PairConfig<DT, BNP, STAGES>;
+  using T = TcTraits<DT>;
+  const CUtensorMapDataType ty = T::ES == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUtensorMap tmA, tmE, tmB;
+  const uint64_t kc = a.K / 2;
+  if (!encode_tensor_map_2d(&tmA, ty, a.values, kc, a.M, kc * T::ES, 128 / T::ES, Cfg::BM,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tensor_map_2d(&tmE, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.meta, a.K / 8, a.M, a.K / 8, 16, Cfg::BM,
+                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_tensor_map_2d(&tmB, ty, a.B, a.K, a.N, a.ldb * T::ES, 128 / T::ES, Cfg::BH,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+    return ST24_ERR_CUDA;
+  CUtensorMap tmC;
+  bool have_c = false;
+  if (a.beta != 0.0f) {
+    const int cs = elem_size(a.c);
+    const CUtensorMapDataType cty = cs == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    have_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && ((a.ldc * cs) % 16 == 0) &&
+             encode_tensor_map_2d(&tmC, cty, a.C, a.M, a.N, a.ldc * cs, Cfg::BM, BNP, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  // The same C with 32 x 32 boxes, for the epilogue's staged chunks.
+  CUtensorMap tmCc;
+  if (have_c) {
+    const int cs = elem_size(a.c);
+    const CUtensorMapDataType cty = cs == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    have_c = encode_tensor_map_2d(&tmCc, cty, a.C, a.M, a.N, a.ldc * cs, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  if (!have_c) tmC = tmCc = tmA;   // unused
+  TcParams p{};
+  p.prefetch_c = have_c ? 1 : 0;
+  p.M = a.M; p.N = a.N; p.K = a.K;
+  p.alpha = a.alpha; p.beta = a.beta;
+  p.C = a.C; p.ldc = a.ldc; p.c_type = a.c;
+  p.row_scale = a.row_scale;
+  p.tiles_m = plan.tiles_m;
+  p.tiles_n = plan.tiles_n;
+  p.group_m = plan.group_m;
+  p.k_iters = plan.k_iters;
+  p.dp_tiles = plan.dp_tiles;
+  p.sk_tiles = plan.sk_tiles;
+  p.a_evict_first = plan.tiles_n == 1 ? 1 : 0;
+  p.a_fixed = (a.flags & ST24_SPMM_FIXED_A) ? 1 : 0;
+  p.partials = static_cast<float*>(a.workspace);
+  p.counters = plan.ws_bytes ? reinterpret_cast<unsigned*>(static_cast<uint8_t*>(a.workspace) +
+                                                          2 * static_cast<size_t>(plan.grid) * plan.partial_bytes)
+                             : nullptr;
+  p.status = dev.status;
+  auto kern = spmm_tc2_kernel<DT, BNP, STAGES>;
+  resident_pairs<DT, BNP, STAGES>(dev.num_sms);   // sets the kernel's shared-memory attribute once
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * plan.grid));
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = 2;
+  attrs[1].val.clusterDim.y = 1;
+  attrs[1].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmE, tmB, tmC, tmCc, p) == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;
+}
+
+}  // namespace tc2
+}  // namespace st24

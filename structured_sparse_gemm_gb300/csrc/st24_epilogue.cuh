@@ -72,19 +72,61 @@ __device__ __forceinline__ void with_float_c_type(int c_type, F&& f) {
   }
 }
 
+// beta * C(m, n0 + j) for the CH columns of a chunk (0 past N), loaded as
+// back-to-back predicated loads.  Called before the chunk's sums are fetched,
+// so the loads' latency overlaps that fetch and few registers are live.
+template <int CT, int CH>
+__device__ __forceinline__ void load_row_chunk_beta_c(const OutParams& p, int64_t m, int64_t n0, float (&bc)[CH]) {
+#pragma unroll
+  for (int j = 0; j < CH; ++j) bc[j] = (n0 + j < p.N) ? c_load<CT>(p.C, (n0 + j) * p.ldc + m) : 0.0f;
+#pragma unroll
+  for (int j = 0; j < CH; ++j) bc[j] = __fmul_rn(p.beta, bc[j]);
+}
+
+// Column chunk [n0, n0 + CH) of output row m from fp32 sums (given as bit
+// patterns) and the chunk's beta * C inputs bc (used only when beta != 0);
+// the epilogue formula and rounding are those of store_out.
+template <int CT, int CH>
+__device__ __forceinline__ void store_row_chunk_bits(const OutParams& p, int64_t m, int64_t n0,
+                                                     const uint32_t (&acc)[CH], const float (&bc)[CH], float factor) {
+  using E = typename std::conditional<CT == kF32, float,
+                                      typename std::conditional<CT == kBF16, __nv_bfloat16, __half>::type>::type;
+  E* out = static_cast<E*>(p.C) + n0 * p.ldc + m;   // one running pointer: few registers live
+  const int64_t cols = p.N - n0;
+#pragma unroll
+  for (int j = 0; j < CH; ++j) {
+    if (j < cols) {
+      float r = __fmul_rn(__uint_as_float(acc[j]), factor);
+      if (p.beta != 0.0f) r = __fadd_rn(r, bc[j]);
+      if constexpr (CT == kF32) *out = r;
+      else if constexpr (CT == kBF16) *out = __float2bfloat16_rn(r);
+      else *out = __float2half_rn(r);
+    }
+    out += p.ldc;
+  }
+}
+
+// beta * C for a chunk staged in shared memory as [32 columns][32 rows] of
+// the output type, row `lane` (32-bit shared address of the chunk).
+template <int CT, int CH>
+__device__ __forceinline__ void staged_beta_c(uint32_t chunk, int lane, float beta, float (&bc)[CH]) {
+#pragma unroll
+  for (int j = 0; j < CH; ++j) {
+    float c;
+    if constexpr (CT == kF32) c = lds_f32(chunk + (j * 32 + lane) * 4);
+    else if constexpr (CT == kBF16) c = __uint_as_float(lds_u16(chunk + (j * 32 + lane) * 2) << 16);
+    else c = __half2float(__ushort_as_half(static_cast<unsigned short>(lds_u16(chunk + (j * 32 + lane) * 2))));
+    bc[j] = __fmul_rn(beta, c);
+  }
+}
+
 // Column chunk [n0, n0 + CH) of output row m from fp32 sums v: every beta*C
-// input of the chunk is loaded before any output is stored (the epilogue
-// formula and rounding are those of store_out).
+// input of the chunk is loaded before any output is stored.
 template <int CT, int CH>
 __device__ __forceinline__ void store_row_chunk(const OutParams& p, int64_t m, int64_t n0, const float (&v)[CH],
                                                 float factor) {
   float bc[CH];
-  if (p.beta != 0.0f) {
-#pragma unroll
-    for (int j = 0; j < CH; ++j) bc[j] = (n0 + j < p.N) ? c_load<CT>(p.C, (n0 + j) * p.ldc + m) : 0.0f;
-#pragma unroll
-    for (int j = 0; j < CH; ++j) bc[j] = __fmul_rn(p.beta, bc[j]);
-  }
+  if (p.beta != 0.0f) load_row_chunk_beta_c<CT, CH>(p, m, n0, bc);
 #pragma unroll
   for (int j = 0; j < CH; ++j) {
     if (n0 + j < p.N) {
@@ -111,6 +153,42 @@ __device__ __forceinline__ void store_out(const OutParams& p, int64_t m, int64_t
     case kF32: static_cast<float*>(p.C)[idx] = r; break;
     case kBF16: static_cast<__nv_bfloat16*>(p.C)[idx] = __float2bfloat16_rn(r); break;
     default: static_cast<__half*>(p.C)[idx] = __float2half_rn(r); break;
+  }
+}
+
+// The contributor that finishes a split tile (stream-K): for output row m,
+// sum the contributors' fp32 partial rows in k order (contributor c_lo first)
+// and apply the epilogue.  Contributor c's partial tile sits at partial slot
+// slot_mul * sch.slot(c, tile) + slot_add, BM x BNW floats column-major, this
+// row at index row.  RCH columns at a time, up to 4 contributors' loads in
+// flight together.  Not inlined: its registers stay out of the main loop's.
+template <int BM, int BNW, int RCH>
+__device__ __noinline__ void reduce_split_row(const OutParams& p, const float* partials, const Schedule& sch,
+                                              int64_t tile, int slot_mul, int slot_add, int64_t c_lo, int64_t c_hi,
+                                              int row, int64_t m, int64_t n_base, float factor) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < BNW; c0 += RCH) {
+    if (n_base + c0 >= p.N) break;
+    float t[RCH];
+    for (int64_t cb = c_lo; cb <= c_hi; cb += 4) {
+      float v[4][RCH];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (cb + u <= c_hi) {
+          const float* src = partials + (slot_mul * sch.slot(cb + u, tile) + slot_add) * (BM * BNW) + row;
+#pragma unroll
+          for (int j = 0; j < RCH; ++j) v[u][j] = __ldcg(src + (c0 + j) * BM);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (cb + u <= c_hi) {
+#pragma unroll
+          for (int j = 0; j < RCH; ++j) t[j] = (cb + u == c_lo) ? v[u][j] : t[j] + v[u][j];
+        }
+      }
+    }
+    with_float_c_type(p.c_type, [&](auto ct) { store_row_chunk<decltype(ct)::value, RCH>(p, m, n_base + c0, t, factor); });
   }
 }
 

@@ -72,6 +72,7 @@ struct StreamKPlan {
   int64_t group_m;         // raster: tiles run in groups of group_m m-tiles, n-tile outer inside a group
   int grid;                // CTAs
   int cluster;             // > 1: each split tile's CTAs form one cluster and reduce through DSMEM
+  int pair;                // tcgen05 CTA-pair tiles (bm = 256): `grid` counts pairs of CTAs
   size_t partial_bytes;    // bytes of one fp32 partial tile
   size_t ws_bytes;         // workspace bytes (0 if no tile is split)
 };

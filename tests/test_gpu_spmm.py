@@ -104,10 +104,12 @@ def test_ragged(kernel, ab, c, M, N, K):
 
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("ab", ["f16", "bf16", "e4m3", "s8"])
-def test_alpha_beta_scale(kernel, ab):
+@pytest.mark.parametrize("N,c", [(48, "bf16"), (300, "bf16"), (300, "f32"), (300, "f16")])
+def test_alpha_beta_scale(kernel, ab, N, c):
+    # N = 300 runs the wide-tile path (two 256 x 224 tiles per pair row, ragged) with C staged per chunk
     if kernel not in kernels_for(ab):
         pytest.skip("no int8 tcgen05 kind on sm_103a")
-    case = inputs.spmm_case(ab, "bf16", 257, 48, 640, alpha=0.5, beta=-0.75, with_scale=True,
+    case = inputs.spmm_case(ab, c, 257, N, 640, alpha=0.5, beta=-0.75, with_scale=True,
                             a_std=0.02 if ab == "e4m3" else 1.0, seed=11)
     check_full(case, kernel=kernel)
 
