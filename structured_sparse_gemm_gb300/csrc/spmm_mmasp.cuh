@@ -69,10 +69,19 @@ struct Config {
   static constexpr int PUSH_BYTES = BN <= 64 ? BM * BN * 4 : 0;   // wide tiles never run in cluster mode
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + PUSH_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   // Narrow (decode) tiles are sized so two CTAs fit on an SM: shared memory
-  // below half the SM's, and at most 168 registers, what the sub-partition
-  // that holds three of the two CTAs' ten warps can give (16384 / 96).
+  // below half the SM's, and registers within what the sub-partition holding
+  // the most of the two CTAs' warps can give (16384 per sub-partition; e.g.
+  // 168 for 2 x 5 warps, 96 for 2 x 9).
   static constexpr bool TWO_PER_SM = BN <= 32;
-  static constexpr int MAX_REGS = TWO_PER_SM ? 168 : (THREADS > 256 ? 168 : 255);
+  // Independent accumulator sets per fragment (k-step ks feeds set ks % KACC,
+  // summed in set order at the end of the tile's k-range).  A warp-level MMA
+  // has a long latency on this GPU: with one set, the narrow tiles' few
+  // fragments form a chain of 4 dependent MMAs per k-block, which bounded
+  // the decode-shaped products.
+  static constexpr int KACC = BN > 32 ? 1 : (WMT_ * WN >= 8 ? 1 : (WMT_ * WN >= 4 ? 2 : 4));
+  static constexpr int WARPS_2 = 2 * (CONSUMERS + 1);
+  static constexpr int REGS_2 = (16384 / ((WARPS_2 + 3) / 4 * 32)) & ~7;
+  static constexpr int MAX_REGS = TWO_PER_SM ? (REGS_2 < 168 ? REGS_2 : 168) : (THREADS > 256 ? 168 : 255);
   static_assert(WN >= 1 && BN % (8 * WARPS_N) == 0, "tile split");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
   static_assert(!TWO_PER_SM || 2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
@@ -267,13 +276,16 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
     int64_t mt, nt;
     tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
     const int64_t m_base = mt * Cfg::BM, n_base = nt * BN;
-    Acc acc[WMT][WN][4];
+    constexpr int KACC = Cfg::KACC;
+    Acc accs[KACC][WMT][WN][4];
 #pragma unroll
-    for (int i = 0; i < WMT; ++i)
+    for (int u = 0; u < KACC; ++u)
 #pragma unroll
-      for (int j = 0; j < WN; ++j)
+      for (int i = 0; i < WMT; ++i)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) acc[i][j][r] = 0;
+        for (int j = 0; j < WN; ++j)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) accs[u][i][j][r] = 0;
 
     bool ok = true;
     for (int64_t kb = kb0; kb < kb1; ++kb) {
@@ -309,11 +321,11 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
 #pragma unroll
           for (int i = 0; i < WMT; ++i) {
             if constexpr (DT == kS8)
-              mma_sp_16864_s8(acc[i][j], a[i], b, e[i][ks]);
+              mma_sp_16864_s8(accs[ks % KACC][i][j], a[i], b, e[i][ks]);
             else if constexpr (DT == kE4M3)
-              mma_sp_16864_e4m3(acc[i][j], a[i], b, e[i][ks]);
+              mma_sp_16864_e4m3(accs[ks % KACC][i][j], a[i], b, e[i][ks]);
             else
-              mma_sp_16832<DT>(acc[i][j], a[i], b, e[i][ks]);
+              mma_sp_16832<DT>(accs[ks % KACC][i][j], a[i], b, e[i][ks]);
           }
         }
       }
@@ -322,6 +334,16 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
       if (++stage == STAGES) { stage = 0; phase ^= 1u; }
     }
     if (!ok) break;
+    // Sum the accumulator sets in set order (a fixed order: deterministic).
+    Acc (&acc)[WMT][WN][4] = accs[0];
+#pragma unroll
+    for (int u = 1; u < KACC; ++u)
+#pragma unroll
+      for (int i = 0; i < WMT; ++i)
+#pragma unroll
+        for (int j = 0; j < WN; ++j)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[i][j][r] += accs[u][i][j][r];
 
     // ---- epilogue ----
     const bool whole = (kb0 == 0 && kb1 == KI);
@@ -563,9 +585,12 @@ st24_status launch_dt_impl(const SpmmArgs& a, const StreamKPlan& plan, const Dev
                       cudaStream_t s) {
   constexpr bool k16 = Traits<DT>::ES == 2;
   switch (plan.bn) {
+    // Decode-shaped tiles.  From N = 9 on, 8 consumer warps of 16 rows each
+    // (half the dependent MMA chain per warp) measured faster; for N <= 8,
+    // 4 warps of 32 rows.
     case 8: return launch_cfg<DT, 8, 1, k16 ? 5 : 4>(a, plan, dev, s);
-    case 16: return launch_cfg<DT, 16, 1, 4>(a, plan, dev, s);
-    case 32: return launch_cfg<DT, 32, 1, 3>(a, plan, dev, s);
+    case 16: return launch_cfg<DT, 16, 1, 4, 1>(a, plan, dev, s);
+    case 32: return launch_cfg<DT, 32, 1, 3, 1>(a, plan, dev, s);
     case 64: return launch_cfg<DT, 64, 1, 5>(a, plan, dev, s);
     default: return launch_cfg<DT, 128, 2, 4>(a, plan, dev, s);
   }

@@ -85,6 +85,7 @@ struct TcConfig {
 struct TcParams : OutParams {
   int64_t K;
   int prefetch_c;          // beta != 0 and C has a tensor map: warm L2 with each tile's C early
+  int c_tma;               // C has a tensor map with 32 x 32 boxes (pair kernel: TMA epilogue)
   int64_t tiles_m, tiles_n, group_m, k_iters, dp_tiles, sk_tiles;
   int a_evict_first;      // A is read by one output tile only: stream it through L2
   int a_fixed;            // A is not written by earlier work on the stream: load it before the dependency wait

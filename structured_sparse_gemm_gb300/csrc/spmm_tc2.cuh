@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(320, 1)
     uint32_t aphase = 0;
     constexpr int CH = Cfg::CH;
     // beta * C from staged chunks when C has a tensor map (else scattered loads).
-    const bool stage_c = p.beta != 0.0f && p.prefetch_c;
+    const bool stage_c = p.beta != 0.0f && p.c_tma;
     uint8_t* my_cbuf = cbuf + q * 2 * Cfg::CBUF_BYTES;
     uint64_t* my_cbar = cbar + 2 * q;
     uint32_t cpar[2] = {0u, 0u};
@@ -323,41 +323,82 @@ __global__ void __launch_bounds__(320, 1)
       const bool whole = (kb0 == 0 && kb1 == KI);
       const bool row_ok = m < p.M;
       const float f = row_ok ? row_factor(p, m) : 0.0f;
-      if (whole) {
+      if (whole && p.c_tma) {
+        // Through shared memory both ways: chunk c of C (32 rows x 32
+        // columns, [column][row]) is staged by TMA one chunk ahead when
+        // beta != 0; the chunk's outputs overwrite it in place and leave by a
+        // TMA store, which clips rows and columns past the output.
         with_float_c_type(p.c_type, [&](auto ct) {
           constexpr int CT = decltype(ct)::value;
           constexpr uint32_t CS = CT == kF32 ? 4u : 2u;
           const int32_t cm = static_cast<int32_t>((2 * mt + rank) * Cfg::BM + 32 * q);   // this warp's 32 rows
-          // Chunk c of C (32 rows x 32 columns) into buffer (c / CH) & 1 of this warp.
-          auto stage_chunk = [&](int c) {
+          auto stage_chunk = [&](int c) {   // lane 0
             const int b = (c / CH) & 1;
-            fence_proxy_async_smem();   // this buffer's earlier reads come before the copy's writes
+            bulk_wait_read<0>();            // the store that last used this buffer has read it
+            fence_proxy_async_smem();
             mbar_arrive_expect_tx(smem_u32(&my_cbar[b]), 32u * 32u * CS);
             tma_load_2d(smem_u32(my_cbuf + b * Cfg::CBUF_BYTES), &tmCc, cm, static_cast<int32_t>(n_base + c),
                         smem_u32(&my_cbar[b]), c_once);
           };
-          if (stage_c && lane == 0) stage_chunk(0);
+          // Buffer b holds chunks c with (c / CH) & 1 == b of every tile; the
+          // previous tile's last stores may still be reading either buffer.
+          if (lane == 0) {
+            if (stage_c)
+              stage_chunk(0);
+            else
+              bulk_wait_read<0>();
+          }
 #pragma unroll 1
           for (int c = 0; c < BNP; c += CH) {
-            const bool in_n = n_base + c < p.N;
-            const bool live = row_ok && in_n;
             if (stage_c && lane == 0 && c + CH < BNP && n_base + c + CH < p.N) stage_chunk(c + CH);
             uint32_t r[CH];
             tmem_ld_x32(tacc + c, r);
             tmem_ld_wait();
+            if (n_base + c >= p.N) continue;   // warp-uniform: nothing of this chunk is in the output
+            const int b = (c / CH) & 1;
+            const uint32_t buf = smem_u32(my_cbuf + b * Cfg::CBUF_BYTES);
             float bc[CH];
-            if (stage_c && in_n) {
-              const int b = (c / CH) & 1;
+            if (stage_c) {
               mbar_wait(smem_u32(&my_cbar[b]), cpar[b], p.status);
               cpar[b] ^= 1u;
-              staged_beta_c<CT, CH>(smem_u32(my_cbuf + b * Cfg::CBUF_BYTES), lane, p.beta, bc);
-              __syncwarp();   // every lane has read this buffer before it is staged again
-            } else if (live && p.beta != 0.0f) {
-              load_row_chunk_beta_c<CT, CH>(p, m, n_base + c, bc);
+              staged_beta_c<CT, CH>(buf, lane, p.beta, bc);   // each lane then overwrites only what it read
+            } else {
+              if (lane == 0) bulk_wait_read<1>();   // the store of two chunks ago has read this buffer
+              __syncwarp();
             }
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+              float o = __fmul_rn(__uint_as_float(r[j]), f);
+              if (p.beta != 0.0f) o = __fadd_rn(o, bc[j]);
+              const uint32_t at = buf + (j * 32 + lane) * CS;
+              if constexpr (CT == kF32) sts_f32(at, o);
+              else if constexpr (CT == kBF16) sts_u16(at, __bfloat16_as_ushort(__float2bfloat16_rn(o)));
+              else sts_u16(at, __half_as_ushort(__float2half_rn(o)));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmCc, cm, static_cast<int32_t>(n_base + c), buf);
+              bulk_commit();
+            }
+          }
+        });
+      } else if (whole) {
+        with_float_c_type(p.c_type, [&](auto ct) {
+          constexpr int CT = decltype(ct)::value;
+#pragma unroll 1
+          for (int c = 0; c < BNP; c += CH) {
+            const bool live = row_ok && n_base + c < p.N;
+            float bc[CH];
+            if (live && p.beta != 0.0f) load_row_chunk_beta_c<CT, CH>(p, m, n_base + c, bc);
+            uint32_t r[CH];
+            tmem_ld_x32(tacc + c, r);
+            tmem_ld_wait();
             if (live) store_row_chunk_bits<CT, CH>(p, m, n_base + c, r, bc, f);
           }
         });
+      }
+      if (whole) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(smem_u32(&tempty_bar[abuf]), 0);
@@ -395,6 +436,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
     }
+    if (lane == 0) bulk_wait_all();   // this warp's output stores have completed
   }
 
   tc_fence_before();
@@ -446,24 +488,22 @@ st24_status launch_pair(const SpmmArgs& a, const StreamKPlan& plan, const Device
       !encode_tensor_map_2d(&tmB, ty, a.B, a.K, a.N, a.ldb * T::ES, 128 / T::ES, Cfg::BH,
                             CU_TENSOR_MAP_SWIZZLE_128B))
     return ST24_ERR_CUDA;
-  CUtensorMap tmC;
-  bool have_c = false;
-  if (a.beta != 0.0f) {
-    const int cs = elem_size(a.c);
-    const CUtensorMapDataType cty = cs == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
-    have_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && ((a.ldc * cs) % 16 == 0) &&
-             encode_tensor_map_2d(&tmC, cty, a.C, a.M, a.N, a.ldc * cs, Cfg::BM, BNP, CU_TENSOR_MAP_SWIZZLE_NONE);
-  }
-  // The same C with 32 x 32 boxes, for the epilogue's staged chunks.
-  CUtensorMap tmCc;
-  if (have_c) {
-    const int cs = elem_size(a.c);
-    const CUtensorMapDataType cty = cs == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
-    have_c = encode_tensor_map_2d(&tmCc, cty, a.C, a.M, a.N, a.ldc * cs, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
-  }
-  if (!have_c) tmC = tmCc = tmA;   // unused
+  // C (element (m, n) at C[n*ldc + m]) as an M-inner 2-D tensor: 32 x 32
+  // boxes for the epilogue's chunks, and a whole-tile box for the L2
+  // prefetch of each tile's C block when beta != 0.
+  CUtensorMap tmC, tmCc;
+  const int cs = elem_size(a.c);
+  const CUtensorMapDataType cty = cs == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const bool c_map = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && ((a.ldc * cs) % 16 == 0) &&
+                     encode_tensor_map_2d(&tmCc, cty, a.C, a.M, a.N, a.ldc * cs, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+  const bool c_prefetch = c_map && a.beta != 0.0f &&
+                          encode_tensor_map_2d(&tmC, cty, a.C, a.M, a.N, a.ldc * cs, Cfg::BM, BNP,
+                                               CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (!c_map) tmCc = tmA;        // unused
+  if (!c_prefetch) tmC = tmA;    // unused
   TcParams p{};
-  p.prefetch_c = have_c ? 1 : 0;
+  p.c_tma = c_map ? 1 : 0;
+  p.prefetch_c = c_prefetch ? 1 : 0;
   p.M = a.M; p.N = a.N; p.K = a.K;
   p.alpha = a.alpha; p.beta = a.beta;
   p.C = a.C; p.ldc = a.ldc; p.c_type = a.c;
