@@ -178,8 +178,9 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
   // loads into the ring straight away.  Before waiting it also warms L2 with
   // the weight tiles of the k-blocks after those (an L2 prefetch cannot
   // observe stale data), so they stream from HBM meanwhile.
+  // The consumers read only shared memory until their epilogue, where they
+  // wait for the previous kernel; their schedule math runs before.
   if (threadIdx.x == 0) grid_launch_dependents();
-  if (warp != Cfg::CONSUMERS) grid_dependency_wait();
 
   if (warp == Cfg::CONSUMERS) {
     // ------------------------------------------------------------ producer
@@ -189,9 +190,14 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
       tma_prefetch_desc(&tmB);
       const uint64_t stream_once = p.a_evict_first ? policy_evict_first() : policy_evict_last();
       const uint64_t reuse = policy_evict_last();
-      uint32_t issued_parity[STAGES];
-      bool issued[STAGES];
-      for (int s = 0; s < STAGES; ++s) issued[s] = false;
+      uint32_t issued = 0, issued_parity = 0;   // per stage (bit s): a copy was issued, and its phase
+      // This CTA's first piece of work, computed before the wait (the
+      // schedule math is off the critical path that starts at the wait).
+      Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, cta);
+      Segment sg;
+      bool have = sch.next(sg);
+      int64_t mt64 = 0, nt64 = 0;
+      if (have) tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt64, nt64);
       int preloaded = 0;   // leading k-blocks whose A and metadata were loaded before the wait
       {
         Schedule pre(KI, p.dp_tiles, p.sk_tiles, G, cta);
@@ -212,8 +218,7 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
               mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
               tma_load_2d(smem_u32(st), &tmA, ka, m0, fb, stream_once);
               tma_load_2d(smem_u32(st + Cfg::A_BYTES + Cfg::B_BYTES), &tmE, ke, m0, fb, stream_once);
-              issued[preloaded] = true;
-              issued_parity[preloaded] = 0;
+              issued |= 1u << preloaded;
               ++preloaded;
             } else {
               tma_prefetch_l2_2d(&tmA, ka, m0);
@@ -228,12 +233,8 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
       uint32_t phase = 0;
       int done = 0;   // k-blocks issued so far
       bool ok = true;
-      Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, cta);
-      Segment sg;
-      while (ok && sch.next(sg)) {
-        const int64_t tile = sg.tile, kb0 = sg.kb0, kb1 = sg.kb1;
-        int64_t mt64, nt64;
-        tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mt64, nt64);
+      while (ok && have) {
+        const int64_t kb0 = sg.kb0, kb1 = sg.kb1;
         const int32_t mt = static_cast<int32_t>(mt64), nt = static_cast<int32_t>(nt64);
         for (int64_t kb = kb0; kb < kb1; ++kb, ++done) {
           const uint32_t fb = smem_u32(&full_bar[stage]);
@@ -246,17 +247,19 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
             tma_load_2d(smem_u32(st), &tmA, ka, mt * Cfg::BM, fb, stream_once);
             tma_load_2d(smem_u32(st + Cfg::A_BYTES + Cfg::B_BYTES), &tmE,
                         static_cast<int32_t>(kb * T::EB), mt * Cfg::BM, fb, stream_once);
-            issued[stage] = true;
-            issued_parity[stage] = phase;
+            issued |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
           tma_load_2d(smem_u32(st + Cfg::A_BYTES), &tmB, kB, nt * BN, fb, reuse);
           tma_load_2d(smem_u32(st + Cfg::A_BYTES + BN * 128), &tmB, kB + 128 / T::ES, nt * BN, fb, reuse);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
+        have = sch.next(sg);
+        if (have) tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt64, nt64);
       }
       // Never leave with copies in flight into this CTA's shared memory.
       for (int s = 0; s < STAGES; ++s)
-        if (issued[s]) mbar_wait(smem_u32(&full_bar[s]), issued_parity[s], p.status);
+        if ((issued >> s) & 1u) mbar_wait(smem_u32(&full_bar[s]), (issued_parity >> s) & 1u, p.status);
     }
     __syncwarp();
     if (p.cluster > 1) cluster_sync();   // the producer warp's part in the in-cluster reduction
@@ -346,6 +349,7 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
           for (int r = 0; r < 4; ++r) acc[i][j][r] += accs[u][i][j][r];
 
     // ---- epilogue ----
+    grid_dependency_wait();   // C, the workspace and the row scales are read or written from here on
     const bool whole = (kb0 == 0 && kb1 == KI);
     bool write_out = whole;
     bool mine[WMT][WN];        // fragments this CTA writes out

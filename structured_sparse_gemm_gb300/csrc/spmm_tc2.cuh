@@ -119,8 +119,11 @@ __global__ void __launch_bounds__(320, 1)
   // As in the one-CTA kernel: inputs are read after the dependency wait,
   // except fixed weights (ST24_SPMM_FIXED_A), whose first stages are loaded
   // before it; L2 is warmed with the weight tiles after those.
+  // Only the producer (B, after its preloads) and the epilogue warps (C, the
+  // workspace, the row scales) touch global memory; they wait for the
+  // previous kernel, the MMA and metadata warps never need to.
   if (threadIdx.x == 0) grid_launch_dependents();
-  if (warp != 0) grid_dependency_wait();
+  if (warp >= 2 && warp <= 5) grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -130,9 +133,7 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tmB);
       const uint64_t stream_once = p.a_evict_first ? policy_evict_first() : policy_evict_last();
       const uint64_t reuse = policy_evict_last();
-      uint32_t issued_parity[STAGES];
-      bool issued[STAGES];
-      for (int s = 0; s < STAGES; ++s) issued[s] = false;
+      uint32_t issued = 0, issued_parity = 0;   // per stage (bit s): a copy was issued, and its phase
       auto load_weights = [&](uint8_t* st, uint32_t fb, int64_t kb, int32_t m0) {
         tma_load_2d(smem_u32(st), &tmA, static_cast<int32_t>(kb * (128 / T::ES)), m0, fb, stream_once);
         uint8_t* se = st + Cfg::A_BYTES + Cfg::B_BYTES;
@@ -154,8 +155,7 @@ __global__ void __launch_bounds__(320, 1)
               const uint32_t fb = smem_u32(&full_bar[preloaded]);
               mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
               load_weights(smem + preloaded * Cfg::STAGE_BYTES, fb, kb, m0);
-              issued[preloaded] = true;
-              issued_parity[preloaded] = 0;
+              issued |= 1u << preloaded;
               ++preloaded;
             } else {
               tma_prefetch_l2_2d(&tmA, static_cast<int32_t>(kb * (128 / T::ES)), m0);
@@ -165,16 +165,18 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
       }
+      // The first piece of work is computed before the wait.
+      Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, pair);
+      Segment sg;
+      bool have = sch.next(sg);
+      int64_t mt64 = 0, nt64 = 0;
+      if (have) tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt64, nt64);
       grid_dependency_wait();
       int stage = 0;
       uint32_t phase = 0;
       int done = 0;
       bool ok = true;
-      Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, pair);
-      Segment sg;
-      while (ok && sch.next(sg)) {
-        int64_t mt64, nt64;
-        tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt64, nt64);
+      while (ok && have) {
         const int32_t m0 = static_cast<int32_t>((2 * mt64 + rank) * Cfg::BM);
         const int32_t n0 = static_cast<int32_t>(nt64 * BNP + rank * Cfg::BH);
         if (p.prefetch_c && sg.kb1 == KI) tma_prefetch_l2_2d(&tmC, m0, static_cast<int32_t>(nt64 * BNP));
@@ -185,17 +187,19 @@ __global__ void __launch_bounds__(320, 1)
             if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) { ok = false; break; }
             mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
             load_weights(st, fb, kb, m0);
-            issued[stage] = true;
-            issued_parity[stage] = phase;
+            issued |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
           const int32_t kB = static_cast<int32_t>(kb * T::BK);
           tma_load_2d(smem_u32(st + Cfg::A_BYTES), &tmB, kB, n0, fb, reuse);
           tma_load_2d(smem_u32(st + Cfg::A_BYTES + Cfg::BH * 128), &tmB, kB + 128 / T::ES, n0, fb, reuse);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
+        have = sch.next(sg);
+        if (have) tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt64, nt64);
       }
       for (int s = 0; s < STAGES; ++s)
-        if (issued[s]) mbar_wait(smem_u32(&full_bar[s]), issued_parity[s], p.status);
+        if ((issued >> s) & 1u) mbar_wait(smem_u32(&full_bar[s]), (issued_parity >> s) & 1u, p.status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader)

@@ -17,6 +17,14 @@
 
 namespace st24 {
 
+// a / b for a >= 0 and b > 0, in 32-bit arithmetic when both fit (64-bit
+// integer division is a long software sequence on the GPU, and this math runs
+// on the producer's critical path at every tile).
+__device__ __forceinline__ int64_t div_nn(int64_t a, int64_t b) {
+  if (((a | b) >> 31) == 0) return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+  return a / b;
+}
+
 struct Segment {
   int64_t tile;
   int64_t kb0, kb1;   // k-blocks [kb0, kb1) of the tile
@@ -28,12 +36,12 @@ struct Segment {
 __device__ __forceinline__ void tile_coords(int64_t tile, int64_t tiles_m, int64_t tiles_n, int64_t group_m,
                                             int64_t& mt, int64_t& nt) {
   const int64_t per_group = group_m * tiles_n;
-  const int64_t g = tile / per_group;
+  const int64_t g = div_nn(tile, per_group);
   const int64_t first = g * group_m;
   const int64_t rows = (tiles_m - first) < group_m ? (tiles_m - first) : group_m;
   const int64_t i = tile - g * per_group;
-  mt = first + i % rows;
-  nt = i / rows;
+  nt = div_nn(i, rows);
+  mt = first + (i - nt * rows);
 }
 
 struct Schedule {
@@ -48,7 +56,7 @@ struct Schedule {
     sk_end = run_begin(cta + 1);
   }
 
-  __device__ __forceinline__ int64_t run_begin(int64_t c) const { return c * sk_iters / G; }
+  __device__ __forceinline__ int64_t run_begin(int64_t c) const { return div_nn(c * sk_iters, G); }
 
   // Next piece of work of this CTA; false when there is none.
   __device__ __forceinline__ bool next(Segment& s) {
@@ -60,7 +68,7 @@ struct Schedule {
       return true;
     }
     if (sk_it < sk_end) {
-      const int64_t local = sk_it / k_iters;
+      const int64_t local = div_nn(sk_it, k_iters);
       s.tile = dp_tiles + local;
       s.kb0 = sk_it - local * k_iters;
       s.kb1 = s.kb0 + (sk_end - sk_it) < k_iters ? s.kb0 + (sk_end - sk_it) : k_iters;
@@ -71,7 +79,7 @@ struct Schedule {
   }
 
   // The CTA whose stream-K run contains iteration u of the tail.
-  __device__ __forceinline__ int64_t owner(int64_t u) const { return ((u + 1) * G - 1) / sk_iters; }
+  __device__ __forceinline__ int64_t owner(int64_t u) const { return div_nn((u + 1) * G - 1, sk_iters); }
   // First and last CTA contributing to stream-K tile `tile`.
   __device__ __forceinline__ int64_t first_cta(int64_t tile) const { return owner((tile - dp_tiles) * k_iters); }
   __device__ __forceinline__ int64_t last_cta(int64_t tile) const {
@@ -80,7 +88,7 @@ struct Schedule {
   // Workspace slot of CTA c's partial of `tile`: 2c for the first tile of its
   // run, 2c + 1 for the last (a run has at most these two partial tiles).
   __device__ __forceinline__ int64_t slot(int64_t c, int64_t tile) const {
-    return 2 * c + ((dp_tiles + run_begin(c) / k_iters) == tile ? 0 : 1);
+    return 2 * c + ((dp_tiles + div_nn(run_begin(c), k_iters)) == tile ? 0 : 1);
   }
 };
 
