@@ -79,6 +79,7 @@ struct Config {
   // fragments form a chain of 4 dependent MMAs per k-block, which bounded
   // the decode-shaped products.
   static constexpr int KACC = BN > 32 ? 1 : (WMT_ * WN >= 8 ? 1 : (WMT_ * WN >= 4 ? 2 : 4));
+  static constexpr bool FRAGS_FIRST = BN <= 8;   // all of a stage's fragments in registers at once
   static constexpr int WARPS_2 = 2 * (CONSUMERS + 1);
   static constexpr int REGS_2 = (16384 / ((WARPS_2 + 3) / 4 * 32)) & ~7;
   static constexpr int MAX_REGS = TWO_PER_SM ? (REGS_2 < 168 ? REGS_2 : 168) : (THREADS > 256 ? 168 : 255);
@@ -92,6 +93,7 @@ struct Params : OutParams {
   int64_t tiles_m, tiles_n, group_m, k_iters, dp_tiles, sk_tiles;
   int a_evict_first;      // A is read by one output tile only: stream it through L2
   int a_fixed;            // A is not written by earlier work on the stream: load it before the dependency wait
+  int b3d;                // tmB is 3-D (128-byte K chunk, row, chunk index): one copy per stage
   int cluster;            // > 1: the CTAs of each split tile form a cluster and reduce in shared memory
   float* partials;       // [2 * gridDim.x][PARTIAL_ELEMS]
   unsigned* counters;    // one per output tile
@@ -250,8 +252,13 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
-          tma_load_2d(smem_u32(st + Cfg::A_BYTES), &tmB, kB, nt * BN, fb, reuse);
-          tma_load_2d(smem_u32(st + Cfg::A_BYTES + BN * 128), &tmB, kB + 128 / T::ES, nt * BN, fb, reuse);
+          if (p.b3d) {
+            // Both 128-byte-wide K chunks of the stage in one copy (3-D map).
+            tma_load_3d(smem_u32(st + Cfg::A_BYTES), &tmB, 0, nt * BN, static_cast<int32_t>(2 * kb), fb, reuse);
+          } else {
+            tma_load_2d(smem_u32(st + Cfg::A_BYTES), &tmB, kB, nt * BN, fb, reuse);
+            tma_load_2d(smem_u32(st + Cfg::A_BYTES + BN * 128), &tmB, kB + 128 / T::ES, nt * BN, fb, reuse);
+          }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         have = sch.next(sg);
@@ -303,6 +310,48 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
         meta_words<DT>(sE, wm * WROWS + i * 16, lane, p.M - m_base - wm * WROWS - i * 16, e[i]);
       const int64_t ks_left = (p.K - kb * T::BK) / T::KSTEP;
       const int ksteps = ks_left < 4 ? static_cast<int>(ks_left) : 4;
+      if constexpr (Cfg::FRAGS_FIRST) {
+        // Narrow tiles: every fragment of the stage is loaded before the
+        // first MMA, so the loads' latencies overlap instead of adding up
+        // k-step by k-step (the inline-asm loads and MMAs keep program order).
+        uint32_t a[4][WMT][4], b[4][WN][4];
+        const int q = lane >> 3, r8 = lane & 7;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          if (ks < ksteps) {
+#pragma unroll
+            for (int i = 0; i < WMT; ++i) {
+              const int row = wm * WROWS + i * 16 + (q & 1) * 8 + r8;
+              const int chunk = ks * 2 + (q >> 1);
+              ldmatrix_x4(sA + row * 128 + ((chunk ^ (row & 7)) << 4), a[ks][i][0], a[ks][i][1], a[ks][i][2],
+                          a[ks][i][3]);
+            }
+#pragma unroll
+            for (int j = 0; j < WN; ++j) {
+              const int n = wn * WN * 8 + j * 8 + r8;
+              const int box = ks >> 1, cb = (ks & 1) * 4 + q;
+              ldmatrix_x4(sB + box * (BN * 128) + n * 128 + ((cb ^ (n & 7)) << 4), b[ks][j][0], b[ks][j][1],
+                          b[ks][j][2], b[ks][j][3]);
+            }
+          }
+        }
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          if (ks < ksteps) {
+#pragma unroll
+            for (int j = 0; j < WN; ++j)
+#pragma unroll
+              for (int i = 0; i < WMT; ++i) {
+                if constexpr (DT == kS8)
+                  mma_sp_16864_s8(accs[ks % KACC][i][j], a[ks][i], b[ks][j], e[i][ks]);
+                else if constexpr (DT == kE4M3)
+                  mma_sp_16864_e4m3(accs[ks % KACC][i][j], a[ks][i], b[ks][j], e[i][ks]);
+                else
+                  mma_sp_16832<DT>(accs[ks % KACC][i][j], a[ks][i], b[ks][j], e[i][ks]);
+              }
+          }
+        }
+      } else {
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         if (ks >= ksteps) break;
@@ -331,6 +380,7 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
               mma_sp_16832<DT>(accs[ks % KACC][i][j], a[i], b, e[i][ks]);
           }
         }
+      }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty_bar[stage]));
@@ -531,7 +581,19 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
       !encode_tensor_map_2d(&tmB, ty, a.B, a.K, a.N, a.ldb * T::ES, 128 / T::ES, BN,
                             CU_TENSOR_MAP_SWIZZLE_128B))
     return ST24_ERR_CUDA;
+  // B as (128-byte K chunk, row, chunk index): a stage's two chunks in one
+  // copy, laid out like the two 2-D boxes (chunk 0's rows, then chunk 1's).
+  // Issuing copies costs the producer thread ~0.1 us each, which paced the
+  // decode-shaped products.
+  CUtensorMap tmB3;
+  const uint64_t bdims[3] = {static_cast<uint64_t>(128 / T::ES), static_cast<uint64_t>(a.N),
+                             static_cast<uint64_t>(a.K / (128 / T::ES))};
+  const uint64_t bstrides[2] = {static_cast<uint64_t>(a.ldb * T::ES), 128};
+  const uint32_t bbox[3] = {128u / T::ES, static_cast<uint32_t>(BN), 2u};
+  const bool b3d = encode_tensor_map_3d(&tmB3, ty, a.B, bdims, bstrides, bbox, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (b3d) tmB = tmB3;
   Params p{};
+  p.b3d = b3d ? 1 : 0;
   p.M = a.M; p.N = a.N; p.K = a.K;
   p.tiles_m = plan.tiles_m;
   p.tiles_n = plan.tiles_n;

@@ -72,6 +72,18 @@ bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, const void
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType type, const void* base, const uint64_t dims[3],
+                          const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  const cuuint64_t st[2] = {strides_bytes[0], strides_bytes[1]};
+  const cuuint32_t b[3] = {box[0], box[1], box[2]};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, type, 3, const_cast<void*>(base), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 StreamKPlan make_stream_k_plan(int bm, int bn, int bk, int64_t M, int64_t N, int64_t K, int num_sms,
                                double a_row_bytes, double b_col_bytes, bool allow_cluster) {
   StreamKPlan pl{};

@@ -108,5 +108,9 @@ st24_status launch_scale_c(const SpmmArgs& a, const DeviceInfo& dev, cudaStream_
 bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base,
                           uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
                           uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+// A 3-D tiled tensor map: dims[0] innermost (contiguous), strides_bytes[i] =
+// stride of dimension i + 1.
+bool encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType type, const void* base, const uint64_t dims[3],
+                          const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swizzle);
 
 }  // namespace st24
