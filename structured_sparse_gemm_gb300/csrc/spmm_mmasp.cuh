@@ -91,7 +91,8 @@ struct Config {
 struct Params : OutParams {
   int64_t K;
   int64_t tiles_m, tiles_n, group_m, k_iters, dp_tiles, sk_tiles;
-  int a_evict_first;      // A is read by one output tile only: stream it through L2
+  int a_evict_first;      // A is streamed once (by the tiles running at the same time): evict it first
+  int b_evict_first;      // B likewise (the raster keeps the A panel resident instead)
   int a_fixed;            // A is not written by earlier work on the stream: load it before the dependency wait
   int b3d;                // tmB is 3-D (128-byte K chunk, row, chunk index): one copy per stage
   int cluster;            // > 1: the CTAs of each split tile form a cluster and reduce in shared memory
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
       tma_prefetch_desc(&tmE);
       tma_prefetch_desc(&tmB);
       const uint64_t stream_once = p.a_evict_first ? policy_evict_first() : policy_evict_last();
-      const uint64_t reuse = policy_evict_last();
+      const uint64_t reuse = p.b_evict_first ? policy_evict_first() : policy_evict_last();
       uint32_t issued = 0, issued_parity = 0;   // per stage (bit s): a copy was issued, and its phase
       // This CTA's first piece of work, computed before the wait (the
       // schedule math is off the critical path that starts at the wait).
@@ -601,7 +602,12 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
   p.k_iters = plan.k_iters;
   p.dp_tiles = plan.dp_tiles;
   p.sk_tiles = plan.sk_tiles;
+  // A is streamed through L2 only when a single tile column reads it; B
+  // stays (it is re-read by every m-tile group).  Marking the operand the
+  // raster streams as evict-first was measured: it raised DRAM re-reads when
+  // the output stream (C) competes for L2.
   p.a_evict_first = plan.tiles_n == 1 ? 1 : 0;
+  p.b_evict_first = 0;
   p.a_fixed = (a.flags & ST24_SPMM_FIXED_A) ? 1 : 0;
   p.cluster = plan.cluster;
   p.alpha = a.alpha; p.beta = a.beta;

@@ -87,7 +87,8 @@ struct TcParams : OutParams {
   int prefetch_c;          // beta != 0 and C has a tensor map: warm L2 with each tile's C early
   int c_tma;               // C has a tensor map with 32 x 32 boxes (pair kernel: TMA epilogue)
   int64_t tiles_m, tiles_n, group_m, k_iters, dp_tiles, sk_tiles;
-  int a_evict_first;      // A is read by one output tile only: stream it through L2
+  int a_evict_first;      // A is streamed once (by the tiles running at the same time): evict it first
+  int b_evict_first;      // B likewise (the raster keeps the A panel resident instead)
   int a_fixed;            // A is not written by earlier work on the stream: load it before the dependency wait
   float* partials;
   unsigned* counters;
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tmE);
       tma_prefetch_desc(&tmB);
       const uint64_t stream_once = p.a_evict_first ? policy_evict_first() : policy_evict_last();
-      const uint64_t reuse = policy_evict_last();
+      const uint64_t reuse = p.b_evict_first ? policy_evict_first() : policy_evict_last();
       uint32_t issued = 0, issued_parity = 0;   // per stage (bit s): a copy was issued, and its phase
       // A and metadata of k-block kb of m-tile mt into stage st (full barrier fb).
       auto load_weights = [&](uint8_t* st, uint32_t fb, int64_t kb, int32_t m0) {
@@ -441,7 +442,12 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
   p.k_iters = plan.k_iters;
   p.dp_tiles = plan.dp_tiles;
   p.sk_tiles = plan.sk_tiles;
+  // A is streamed through L2 only when a single tile column reads it; B
+  // stays (it is re-read by every m-tile group).  Marking the operand the
+  // raster streams as evict-first was measured: it raised DRAM re-reads when
+  // the output stream (C) competes for L2.
   p.a_evict_first = plan.tiles_n == 1 ? 1 : 0;
+  p.b_evict_first = 0;
   p.a_fixed = (a.flags & ST24_SPMM_FIXED_A) ? 1 : 0;
   p.partials = static_cast<float*>(a.workspace);
   p.counters = plan.ws_bytes ? reinterpret_cast<unsigned*>(static_cast<uint8_t*>(a.workspace) +

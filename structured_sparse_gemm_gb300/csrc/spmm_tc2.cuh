@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tmE);
       tma_prefetch_desc(&tmB);
       const uint64_t stream_once = p.a_evict_first ? policy_evict_first() : policy_evict_last();
-      const uint64_t reuse = policy_evict_last();
+      const uint64_t reuse = p.b_evict_first ? policy_evict_first() : policy_evict_last();
       uint32_t issued = 0, issued_parity = 0;   // per stage (bit s): a copy was issued, and its phase
       auto load_weights = [&](uint8_t* st, uint32_t fb, int64_t kb, int32_t m0) {
         tma_load_2d(smem_u32(st), &tmA, static_cast<int32_t>(kb * (128 / T::ES)), m0, fb, stream_once);
@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(320, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmCc, cm, static_cast<int32_t>(n_base + c), buf);
+              tma_store_2d(&tmCc, cm, static_cast<int32_t>(n_base + c), buf, c_once);   // the output streams through L2
               bulk_commit();
             }
           }
@@ -518,7 +518,12 @@ st24_status launch_pair(const SpmmArgs& a, const StreamKPlan& plan, const Device
   p.k_iters = plan.k_iters;
   p.dp_tiles = plan.dp_tiles;
   p.sk_tiles = plan.sk_tiles;
+  // A is streamed through L2 only when a single tile column reads it; B
+  // stays (it is re-read by every m-tile group).  Marking the operand the
+  // raster streams as evict-first was measured: it raised DRAM re-reads when
+  // the output stream (C) competes for L2.
   p.a_evict_first = plan.tiles_n == 1 ? 1 : 0;
+  p.b_evict_first = 0;
   p.a_fixed = (a.flags & ST24_SPMM_FIXED_A) ? 1 : 0;
   p.partials = static_cast<float*>(a.workspace);
   p.counters = plan.ws_bytes ? reinterpret_cast<unsigned*>(static_cast<uint8_t*>(a.workspace) +

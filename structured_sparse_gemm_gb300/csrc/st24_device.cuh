@@ -326,10 +326,10 @@ __device__ __forceinline__ void tc_cp_128x128b(uint32_t taddr, uint64_t desc) {
 // 2-D tiled store of a box from shared memory to global memory at (x, y);
 // parts of the box outside the tensor are not written.  Completion is
 // tracked per thread with bulk groups.
-__device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x, int32_t y, uint32_t src) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x, int32_t y, uint32_t src, uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(
                    reinterpret_cast<uint64_t>(tmap)),
-               "r"(x), "r"(y), "r"(src)
+               "r"(x), "r"(y), "r"(src), "l"(policy)
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
