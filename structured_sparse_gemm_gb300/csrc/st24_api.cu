@@ -104,11 +104,17 @@ StreamKPlan make_stream_k_plan(int bm, int bn, int bk, int64_t M, int64_t N, int
   pl.grid = static_cast<int>(grid > 0 ? grid : 1);
   // Whole waves of tiles run data-parallel; the remainder plus one wave (so
   // that each of its tiles is split over only one or two CTAs) runs stream-K.
+  // With many waves and a nearly full last one, whole tiles throughout:
+  // a stream-K tail costs each split tile a partial-tile round trip through
+  // the workspace, more than the last wave's idle share (measured on
+  // 11008x4096, N = 4096: 10.75 waves of CTA pairs).
   if (tiles <= pl.grid) {
     pl.sk_tiles = tiles;
   } else {
     const int64_t rem = tiles % pl.grid;
-    pl.sk_tiles = rem == 0 ? 0 : rem + pl.grid;
+    const int64_t waves = (tiles + pl.grid - 1) / pl.grid;
+    const bool tail_cheap = rem == 0 || (pl.grid - rem) * 100 <= 3 * waves * pl.grid;   // idle share <= 3%
+    pl.sk_tiles = tail_cheap ? 0 : rem + pl.grid;
   }
   pl.dp_tiles = tiles - pl.sk_tiles;
   // Raster.  Consecutive tiles run at the same time; keep one operand's panel
