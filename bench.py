@@ -347,14 +347,32 @@ def run_e2e(args, w, layers, stream):
         h2d += hA.numel() * hA.element_size()
         host.append((hA, hX))
 
+    # Uploads run on their own stream, layer by layer, so each layer's weight
+    # copy overlaps the work already queued (the previous layers' prune and
+    # the previous step's products): the host link, not the GPU, bounds a step.
+    copy_stream = torch.cuda.Stream(device=stream.device)
+    copied = [torch.cuda.Event() for _ in layers]
+    pruned = [torch.cuda.Event() for _ in layers]
+    products_done = torch.cuda.Event()
+    first = [True]
+
     def step():
-        with torch.cuda.stream(stream):
-            for L, (hA, hX) in zip(layers, host):
+        for i, (L, (hA, hX)) in enumerate(zip(layers, host)):
+            with torch.cuda.stream(copy_stream):
+                if not first[0]:
+                    copy_stream.wait_event(pruned[i])         # the last step's prune has read A
                 L["A"].copy_(hA, non_blocking=True)
+                if not first[0]:
+                    copy_stream.wait_event(products_done)     # the last step's products have read X
                 for (X, Y, ws), (hx, hy) in zip(L["acts"], hX):
                     X.copy_(hx, non_blocking=True)
-            for L in layers:
+                copied[i].record(copy_stream)
+        first[0] = False
+        with torch.cuda.stream(stream):
+            for i, L in enumerate(layers):
+                stream.wait_event(copied[i])
                 st.st24_prune_compress(L["A"], L["values"], L["meta"])
+                pruned[i].record(stream)
             for ni in range(len(w["Ns"])):
                 for li, L in enumerate(layers):
                     X, Y, ws = L["acts"][ni]
@@ -363,6 +381,7 @@ def run_e2e(args, w, layers, stream):
                     fixed = args.fixed_a and not (ni == 0 and li == 0 and len(layers) == 1)
                     st.st24_spmm(L["values"], L["meta"], X, Y, K=L["K"], beta=w["beta"], row_scale=L["scale"],
                                  workspace=ws, fixed_a=fixed)
+            products_done.record(stream)
             for L, (hA, hX) in zip(layers, host):
                 for (X, Y, ws), (hx, hy) in zip(L["acts"], hX):
                     hy.copy_(Y, non_blocking=True)
@@ -372,9 +391,10 @@ def run_e2e(args, w, layers, stream):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    copy_stream.wait_event(e0)    # no timed upload starts before the timed region
     for _ in range(args.steps):
         step()
-    e1.record(stream)
+    e1.record(stream)             # each step ends with its outputs' download on `stream`
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     return ms, h2d, d2h
