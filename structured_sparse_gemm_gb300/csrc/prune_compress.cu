@@ -175,26 +175,45 @@ __device__ __forceinline__ bool compress_piece_lanes(const uint4 in, uint2& out,
     out = make_uint2(prmt(v0, v1, 0x5410), prmt(v0, v1, 0x7632));
     meta_bits = (nib & 0xFu) | ((nib >> 12) & 0xF0u);
     return true;
-  } else if constexpr (DT == kE4M3) {
-    // 4x4 byte transpose: x[i] = element i of groups 0..3 (lane g = group g).
+  } else {
+    // 8-bit types, 8-bit lanes: 4x4 byte transpose, x[i] = element i of
+    // groups 0..3 (lane g = group g).
     const uint32_t t0 = prmt(in.x, in.y, 0x5140), t1 = prmt(in.x, in.y, 0x7362);
     const uint32_t t2 = prmt(in.z, in.w, 0x5140), t3 = prmt(in.z, in.w, 0x7362);
     const uint32_t x[4] = {prmt(t0, t2, 0x5410), prmt(t0, t2, 0x7632), prmt(t1, t3, 0x5410),
                            prmt(t1, t3, 0x7632)};
-    // |x| order is the order of the low 7 bits; 0x7F, the only NaN
-    // magnitude, is above every number and ties with itself.
     uint32_t k[4];
+    bool lanes8 = true;
+    if constexpr (DT == kE4M3) {
+      // |x| order is the order of the low 7 bits; 0x7F, the only NaN
+      // magnitude, is above every number and ties with itself.
 #pragma unroll
-    for (int i = 0; i < 4; ++i) k[i] = x[i] & 0x7F7F7F7Fu;
-    uint32_t v0, v1, nib;
-    select_lanes<8>(k, x, v0, v1, nib);
-    out = make_uint2(prmt(v0, v1, 0x5140), prmt(v0, v1, 0x7362));
-    const uint32_t t = nib | (nib >> 4);   // bytes 0 and 2: two nibbles each
-    meta_bits = prmt(t, 0, 0x4420) & 0xFFFFu;
-    return true;
-  } else {
-    // int8: |-128| = 128 needs 8 bits, so 16-bit lanes, two groups per pass;
-    // each element sign-extended into its lane.
+      for (int i = 0; i < 4; ++i) k[i] = x[i] & 0x7F7F7F7Fu;
+    } else {
+      // int8: |v| fits in 7 bits unless v = -128 (a 0x80 byte); such pieces
+      // take 16-bit lanes below.
+      uint32_t has_min = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t y = x[i] ^ 0x80808080u;   // 0x80 bytes become zero bytes
+        has_min |= (y - 0x01010101u) & ~y & 0x80808080u;
+        const uint32_t neg = prmt(x[i], 0, 0xBA98);   // all-ones in negative bytes
+        k[i] = (x[i] ^ neg) + (neg & 0x01010101u);
+      }
+      lanes8 = has_min == 0;
+    }
+    if (lanes8) {
+      uint32_t v0, v1, nib;
+      select_lanes<8>(k, x, v0, v1, nib);
+      out = make_uint2(prmt(v0, v1, 0x5140), prmt(v0, v1, 0x7362));
+      const uint32_t t = nib | (nib >> 4);   // bytes 0 and 2: two nibbles each
+      meta_bits = prmt(t, 0, 0x4420) & 0xFFFFu;
+      return true;
+    }
+  }
+  if constexpr (DT == kS8) {
+    // int8 with a -128: |-128| = 128 needs 8 bits, so 16-bit lanes, two
+    // groups per pass; each element sign-extended into its lane.
     const uint32_t w[4] = {in.x, in.y, in.z, in.w};
     uint32_t pairs[2];
     meta_bits = 0;
@@ -216,6 +235,7 @@ __device__ __forceinline__ bool compress_piece_lanes(const uint4 in, uint2& out,
     out = make_uint2(pairs[0], pairs[1]);
     return true;
   }
+  return false;   // not reached: e4m3 always takes the 8-bit lanes
 }
 
 template <int ES>

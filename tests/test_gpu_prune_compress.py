@@ -75,6 +75,16 @@ def test_ties_zeros_nan(dt):
     check(W)
 
 
+def test_int8_extremes():
+    # |-128| = 128 does not fit the 8-bit lanes of the fast selection: pieces holding a -128 take the
+    # 16-bit lanes, the others the 8-bit ones; both must follow the same tie and magnitude rule
+    g = torch.Generator().manual_seed(3)
+    vals = torch.tensor([-128, -127, -1, 0, 1, 127], dtype=torch.int8)
+    W = vals[torch.randint(0, len(vals), (96, 1024), generator=g)]
+    W[:48, :512] = torch.where(W[:48, :512] == -128, torch.tensor(-127, dtype=torch.int8), W[:48, :512])
+    check(W)
+
+
 def test_empty_is_noop():
     W = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
     st.st24_prune_compress(W, torch.empty(0, device=DEV), torch.empty(0, device=DEV))
