@@ -458,7 +458,7 @@ def main():
     ap.add_argument("--impl", default="st24", choices=["st24", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "tcgen05", "mma_sp"],
+    ap.add_argument("--kernel", default="auto", choices=["auto", "tcgen05", "mma_sp", "mma_sp_direct"],
                     help="SpMM kernel family (auto = what st24_spmm picks)")
     ap.add_argument("--no-fixed-a", dest="fixed_a", action="store_false",
                     help="do not declare the weights fixed (ST24_SPMM_FIXED_A) to the products")

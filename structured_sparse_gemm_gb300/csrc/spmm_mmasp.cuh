@@ -184,6 +184,10 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
   // The consumers read only shared memory until their epilogue, where they
   // wait for the previous kernel; their schedule math runs before.
   if (threadIdx.x == 0) grid_launch_dependents();
+  // Cluster mode: every thread arrives once here and waits once before its
+  // part in the in-cluster reduction, so no CTA stores into another's shared
+  // memory before that CTA has started.
+  if (p.cluster > 1) cluster_arrive_relaxed();
 
   if (warp == Cfg::CONSUMERS) {
     // ------------------------------------------------------------ producer
@@ -270,7 +274,10 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
         if ((issued >> s) & 1u) mbar_wait(smem_u32(&full_bar[s]), (issued_parity >> s) & 1u, p.status);
     }
     __syncwarp();
-    if (p.cluster > 1) cluster_sync();   // the producer warp's part in the in-cluster reduction
+    if (p.cluster > 1) {   // the producer warp's part in the in-cluster reduction
+      cluster_wait();
+      cluster_sync();
+    }
     return;
   }
 
@@ -422,6 +429,7 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
       const int owned_max = (F + cs - 1) / cs;
       const int rank = static_cast<int>(cluster_ctarank());
       float4* slots = push_slots;                            // [cluster][owned_max][32 lanes]
+      cluster_wait();                                        // every CTA of the cluster has started
 #pragma unroll
       for (int i = 0; i < WMT; ++i)
 #pragma unroll
@@ -564,7 +572,10 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
   }
   // A wait that ran out of time skipped the reduction: still meet the peers
   // at the cluster barrier.
-  if (p.cluster > 1 && cluster_done == 0) cluster_sync();
+  if (p.cluster > 1 && cluster_done == 0) {
+    cluster_wait();
+    cluster_sync();
+  }
 }
 
 template <int DT, int BN, int WARPS_N, int STAGES, int WMT = 2>

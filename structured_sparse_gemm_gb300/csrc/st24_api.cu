@@ -165,19 +165,21 @@ namespace {
 //  * int8: the warp-level kernel (there is no int8 tcgen05 kind on sm_103a).
 //  * fp8: tcgen05 always; the warp-level e4m3 sparse MMA runs at ~1/50 of the
 //    16-bit one on this GPU.
-//  * 16-bit: the warp-level kernel while the product is bound by streaming
-//    the compressed A from HBM (2N flops per logical weight over 1.125 bytes,
-//    at most 64 flop/B: N <= 32), where it has less fixed latency per launch;
-//    tcgen05 beyond.
+//  * 16-bit: while the product is bound by streaming the compressed A from
+//    HBM (2N flops per logical weight over 1.125 bytes, at most 64 flop/B:
+//    N <= 32), the warp-level kernel that loads the weights straight into
+//    registers (the least fixed latency per launch; measured faster than the
+//    TMA-ring one at every decode width); tcgen05 beyond.
 int resolve_kernel(int requested, int ab, int64_t N) {
   if (requested != ST24_KERNEL_AUTO) return requested;
   if (ab == kS8) return ST24_KERNEL_MMA_SP;
   if (ab == kE4M3) return ST24_KERNEL_TCGEN05;
   const double intensity = 2.0 * static_cast<double>(N) / (elem_size(ab) / 2.0 + 0.125);
-  return intensity <= 64.0 ? ST24_KERNEL_MMA_SP : ST24_KERNEL_TCGEN05;
+  return intensity <= 64.0 ? ST24_KERNEL_MMA_SP_DIRECT : ST24_KERNEL_TCGEN05;
 }
 
 StreamKPlan plan_for(int kernel, const SpmmArgs& a, int num_sms) {
+  if (kernel == ST24_KERNEL_MMA_SP_DIRECT) return StreamKPlan{};   // one launch shape, no workspace
   return kernel == ST24_KERNEL_TCGEN05 ? plan_spmm_tc(a, num_sms) : plan_spmm_mmasp(a, num_sms);
 }
 
@@ -275,7 +277,8 @@ st24_status st24_spmm_ex(st24_kernel kernel, unsigned flags, st24_dtype ab_type,
                          int64_t N, int64_t K, float alpha, const void* A_values, const void* A_meta, const void* B,
                          int64_t ldb, float beta, void* C, int64_t ldc, const float* row_scale,
                          void* workspace, size_t ws_bytes, void* stream) {
-  if (kernel != ST24_KERNEL_AUTO && kernel != ST24_KERNEL_TCGEN05 && kernel != ST24_KERNEL_MMA_SP)
+  if (kernel != ST24_KERNEL_AUTO && kernel != ST24_KERNEL_TCGEN05 && kernel != ST24_KERNEL_MMA_SP &&
+      kernel != ST24_KERNEL_MMA_SP_DIRECT)
     return ST24_ERR_INVALID_ARG;
   if (flags & ~static_cast<unsigned>(ST24_SPMM_FIXED_A)) return ST24_ERR_INVALID_ARG;
   SpmmArgs a{};
@@ -300,10 +303,12 @@ st24_status st24_spmm_ex(st24_kernel kernel, unsigned flags, st24_dtype ab_type,
   if (st != ST24_OK || M == 0 || N == 0) return st;
   const int k = resolve_kernel(kernel, ab_type, N);
   if (k == ST24_KERNEL_TCGEN05 && ab_type == ST24_S8) return ST24_ERR_UNSUPPORTED;
+  if (k == ST24_KERNEL_MMA_SP_DIRECT && !direct_applies(a)) return ST24_ERR_UNSUPPORTED;
   const DeviceInfo* dev = current_device_info();
   if (!dev) return ST24_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return launch_scale_c(a, *dev, s);
+  if (k == ST24_KERNEL_MMA_SP_DIRECT) return launch_spmm_direct(a, *dev, s);
   const StreamKPlan plan = plan_for(k, a, dev->num_sms);
   if (plan.ws_bytes > 0 && (!workspace || ws_bytes < plan.ws_bytes || !aligned(workspace, 16)))
     return ST24_ERR_WORKSPACE;

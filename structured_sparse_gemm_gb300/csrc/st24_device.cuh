@@ -422,6 +422,14 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The two halves of a cluster barrier phase: every thread of every CTA of the
+// cluster arrives once, then waits.  Arriving at the start of a kernel and
+// waiting just before the first access to another CTA's shared memory makes
+// sure that CTA has started, at almost no cost.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 // A 16-byte load from the same shared-memory offset in CTA `rank` of the cluster.
 __device__ __forceinline__ float4 ld_shared_cluster_f4(const void* local, uint32_t rank) {
   uint32_t remote;

@@ -98,12 +98,24 @@ def test_spmm_rejects_bad_arguments(lib):
     assert call(M=0, v=None, e=None, B=None, C=None) == 0    # empty: no-op
 
 
+def test_direct_kernel_rejects_what_it_does_not_cover(lib):
+    # the register-direct family takes 16-bit inputs with 1 <= N <= 32 only
+    def call(ab, c, N):
+        return lib.st24_spmm_ex(st.KERNEL_MMA_SP_DIRECT, 0, ab, c, 128, N, 256, 1.0, FAKE, FAKE, FAKE, 256, 0.0,
+                                FAKE, 128, None, None, 0, None)
+
+    assert call(st.S8, st.S32, 8) == 2
+    assert call(st.E4M3, st.BF16, 8) == 2
+    assert call(st.BF16, st.BF16, 33) == 2
+
+
 def test_spmm_ex_rejects_unknown_kernel_and_flags(lib):
     def call(kernel=0, flags=0):
         return lib.st24_spmm_ex(kernel, flags, st.BF16, st.BF16, 128, 8, 256, 1.0, FAKE, FAKE, FAKE, 256, 0.0,
                                 FAKE, 128, None, None, 0, None)
 
-    assert call(kernel=3) == 1
+    assert call(kernel=4) == 1
+    assert call(kernel=-1) == 1
     assert call(flags=2) == 1
     assert call(flags=1 << 31) == 1
     assert call(kernel=7, flags=1) == 1

@@ -114,6 +114,34 @@ def test_alpha_beta_scale(kernel, ab, N, c):
     check_full(case, kernel=kernel)
 
 
+# The register-direct family (16-bit inputs, N <= 32): ragged rows, every
+# split of K over a cluster (1, 2, 4, 8 CTAs), several 512-K rounds per CTA,
+# K ranges that end inside a round, and each B width it stages (8, 16, 32).
+DIRECT_SHAPES = [(129, 1, 128), (200, 5, 384), (300, 16, 640), (64, 32, 512), (385, 24, 1280),
+                 (130, 17, 4224), (1000, 9, 8192), (77, 8, 2048)]
+
+
+@pytest.mark.parametrize("ab", ["f16", "bf16"])
+@pytest.mark.parametrize("c", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", DIRECT_SHAPES)
+def test_direct_ragged(ab, c, M, N, K):
+    check_full(inputs.spmm_case(ab, c, M, N, K, seed=M + N + K), kernel="mma_sp_direct")
+
+
+@pytest.mark.parametrize("ab", ["f16", "bf16"])
+@pytest.mark.parametrize("N,c", [(1, "bf16"), (13, "f16"), (32, "f32")])
+def test_direct_alpha_beta_scale(ab, N, c):
+    case = inputs.spmm_case(ab, c, 257, N, 640, alpha=0.5, beta=-0.75, with_scale=True, seed=11)
+    check_full(case, kernel="mma_sp_direct")
+
+
+def test_direct_rejects_int8_and_wide_n():
+    for case in (inputs.spmm_case("s8", "s32", 128, 16, 256, seed=1), inputs.spmm_case("bf16", "bf16", 128, 33, 256)):
+        with pytest.raises(st.St24Error) as e:
+            gpu_run(case, kernel="mma_sp_direct")
+        assert e.value.status == 2
+
+
 @pytest.mark.parametrize("N", [8, 200])
 def test_int8_int32_bit_exact(N):
     case = inputs.spmm_case("s8", "s32", 384, N, 1024, seed=N)
@@ -144,14 +172,14 @@ def test_deterministic_and_workspace_reuse():
 
 # ---- the workloads at their full sizes -------------------------------------------
 
-@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kernel", KERNELS + ["mma_sp_direct"])
 @pytest.mark.parametrize("N", inputs.DECODE_NS)
 def test_decode_bf16_full(kernel, N):
     check_full(inputs.decode_bf16(N), kernel=kernel)
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
-@pytest.mark.parametrize("N", [1, 32, 200])
+@pytest.mark.parametrize("kernel,N", [(k, n) for k in KERNELS for n in (1, 32, 200)] +
+                         [("mma_sp_direct", 1), ("mma_sp_direct", 32)])
 def test_fixed_weights_back_to_back(kernel, N):
     """Products over several weights enqueued back to back with ST24_SPMM_FIXED_A
     (weight tiles loaded while the previous product still runs) equal the same
