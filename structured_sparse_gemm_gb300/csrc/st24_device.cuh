@@ -429,7 +429,39 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+// 16 bytes into the shared memory of CTA `rank` of the cluster (same offset as
+// `local_dst`), counted as complete_tx bytes on that CTA's barrier at the
+// offset of `local_bar`.  Asynchronous: the sender does not wait.
+__device__ __forceinline__ void st_async_cluster_f4(const void* local_dst, const void* local_bar, uint32_t rank,
+                                                    float4 v) {
+  uint32_t rd, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rd) : "r"(smem_u32(local_dst)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(local_bar)), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(rd),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rb)
+               : "memory");
+}
+
+// Bulk copy (TMA, no tensor map) of `bytes` (a multiple of 16, both addresses
+// 16-byte aligned) from global memory into this CTA's shared memory,
+// completing as tx bytes on the barrier at shared address `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// cp.async of 16 bytes, global -> shared, cached in L2 only.
+__device__ __forceinline__ void cp_async_cg16(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sdst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 // A 16-byte load from the same shared-memory offset in CTA `rank` of the cluster.
 __device__ __forceinline__ float4 ld_shared_cluster_f4(const void* local, uint32_t rank) {
   uint32_t remote;
