@@ -79,12 +79,14 @@ typedef enum st24_status {
 
 /* Kernel families st24_spmm_ex can be asked to use. */
 typedef enum st24_kernel {
-    ST24_KERNEL_AUTO = 0,     /* what st24_spmm uses: MMA_SP_DIRECT for 16-bit inputs with N <= 32
-                                 (HBM-bound), MMA_SP for int8, TCGEN05 otherwise (always for e4m3) */
+    ST24_KERNEL_AUTO = 0,     /* what st24_spmm uses: for 16-bit inputs with N <= 32 (HBM-bound)
+                                 MMA_SP_DIRECT when its grid fits in one wave, else MMA_SP; MMA_SP
+                                 for int8; TCGEN05 otherwise (always for e4m3) */
     ST24_KERNEL_TCGEN05 = 1,  /* tcgen05.mma.sp with TMEM accumulators (f16, bf16, e4m3 only) */
     ST24_KERNEL_MMA_SP = 2,   /* warp-level mma.sp fed by a TMA ring in shared memory (all input types) */
     ST24_KERNEL_MMA_SP_DIRECT = 3  /* warp-level mma.sp with the weights loaded straight into registers
-                                      (f16, bf16 with 1 <= N <= 32 only; no workspace) */
+                                      (1 <= N <= 32 only; 8-bit inputs widened exactly to f16; no
+                                      workspace) */
 } st24_kernel;
 
 /* Option bits for st24_spmm_ex (OR them together; 0 = none). */
@@ -192,8 +194,7 @@ ST24_API st24_status st24_spmm(st24_dtype ab_type, st24_dtype c_type, int64_t M,
  * st24_spmm with options: an explicitly chosen kernel family (for testing one
  * family against another, or a family against the oracle) and `flags`, a set
  * of st24_spmm_flags bits.  ST24_KERNEL_TCGEN05 with ab_type ST24_S8, and
- * ST24_KERNEL_MMA_SP_DIRECT with an 8-bit ab_type or N > 32, return
- * ST24_ERR_UNSUPPORTED.  Arguments, workspace and results are as for
+ * ST24_KERNEL_MMA_SP_DIRECT with N > 32, return ST24_ERR_UNSUPPORTED.  Arguments, workspace and results are as for
  * st24_spmm (which is st24_spmm_ex with ST24_KERNEL_AUTO and no flags);
  * st24_spmm_workspace_bytes covers every family.  An unknown `kernel` or an
  * unknown flag bit returns ST24_ERR_INVALID_ARG.

@@ -167,15 +167,20 @@ namespace {
 //    16-bit one on this GPU.
 //  * 16-bit: while the product is bound by streaming the compressed A from
 //    HBM (2N flops per logical weight over 1.125 bytes, at most 64 flop/B:
-//    N <= 32), the warp-level kernel that loads the weights straight into
-//    registers (the least fixed latency per launch; measured faster than the
-//    TMA-ring one at every decode width); tcgen05 beyond.
-int resolve_kernel(int requested, int ab, int64_t N) {
+//    N <= 32), a warp-level kernel: the one that loads the weights straight
+//    into registers when its grid fits in one wave (the least fixed latency
+//    per launch; measured faster than the TMA-ring one at every decode width
+//    of a 4096 x 4096 weight), else the TMA-ring one, whose persistent grid
+//    pipelines across tiles; tcgen05 beyond.  (For 8-bit inputs the
+//    register-direct kernel measured slower than the families above, so it
+//    is used only when asked for.)
+int resolve_kernel(int requested, const SpmmArgs& a, int num_sms) {
   if (requested != ST24_KERNEL_AUTO) return requested;
-  if (ab == kS8) return ST24_KERNEL_MMA_SP;
-  if (ab == kE4M3) return ST24_KERNEL_TCGEN05;
-  const double intensity = 2.0 * static_cast<double>(N) / (elem_size(ab) / 2.0 + 0.125);
-  return intensity <= 64.0 ? ST24_KERNEL_MMA_SP_DIRECT : ST24_KERNEL_TCGEN05;
+  if (a.ab == kS8) return ST24_KERNEL_MMA_SP;
+  if (a.ab == kE4M3) return ST24_KERNEL_TCGEN05;
+  const double intensity = 2.0 * static_cast<double>(a.N) / (elem_size(a.ab) / 2.0 + 0.125);
+  if (intensity > 64.0) return ST24_KERNEL_TCGEN05;
+  return direct_one_wave(a, num_sms) ? ST24_KERNEL_MMA_SP_DIRECT : ST24_KERNEL_MMA_SP;
 }
 
 StreamKPlan plan_for(int kernel, const SpmmArgs& a, int num_sms) {
@@ -186,7 +191,7 @@ StreamKPlan plan_for(int kernel, const SpmmArgs& a, int num_sms) {
 }  // namespace
 
 StreamKPlan st24::plan_auto(const SpmmArgs& a, int num_sms) {
-  return plan_for(resolve_kernel(ST24_KERNEL_AUTO, a.ab, a.N), a, num_sms);
+  return plan_for(resolve_kernel(ST24_KERNEL_AUTO, a, num_sms), a, num_sms);
 }
 
 st24_status st24::check_spmm_args(const SpmmArgs& a) {
@@ -301,11 +306,11 @@ st24_status st24_spmm_ex(st24_kernel kernel, unsigned flags, st24_dtype ab_type,
   a.ws_bytes = ws_bytes;
   st24_status st = check_spmm_args(a);
   if (st != ST24_OK || M == 0 || N == 0) return st;
-  const int k = resolve_kernel(kernel, ab_type, N);
-  if (k == ST24_KERNEL_TCGEN05 && ab_type == ST24_S8) return ST24_ERR_UNSUPPORTED;
-  if (k == ST24_KERNEL_MMA_SP_DIRECT && !direct_applies(a)) return ST24_ERR_UNSUPPORTED;
+  if (kernel == ST24_KERNEL_TCGEN05 && ab_type == ST24_S8) return ST24_ERR_UNSUPPORTED;
+  if (kernel == ST24_KERNEL_MMA_SP_DIRECT && !direct_applies(a)) return ST24_ERR_UNSUPPORTED;
   const DeviceInfo* dev = current_device_info();
   if (!dev) return ST24_ERR_CUDA;
+  const int k = resolve_kernel(kernel, a, dev->num_sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return launch_scale_c(a, *dev, s);
   if (k == ST24_KERNEL_MMA_SP_DIRECT) return launch_spmm_direct(a, *dev, s);

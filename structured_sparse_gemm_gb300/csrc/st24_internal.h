@@ -96,8 +96,10 @@ StreamKPlan plan_spmm_mmasp(const SpmmArgs& a, int num_sms);
 st24_status launch_spmm_mmasp(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev,
                               cudaStream_t stream);
 
-// The register-direct mma.sp path: f16, bf16 with N <= 32 (no workspace).
+// The register-direct mma.sp path: N <= 32, every input type (no workspace).
 bool direct_applies(const SpmmArgs& a);
+// Whether its grid (two CTAs per SM) runs in one wave on num_sms SMs.
+bool direct_one_wave(const SpmmArgs& a, int num_sms);
 st24_status launch_spmm_direct(const SpmmArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
 // The tcgen05 (5th-generation tensor core) path: f16, bf16, e4m3.

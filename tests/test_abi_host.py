@@ -99,14 +99,13 @@ def test_spmm_rejects_bad_arguments(lib):
 
 
 def test_direct_kernel_rejects_what_it_does_not_cover(lib):
-    # the register-direct family takes 16-bit inputs with 1 <= N <= 32 only
+    # the register-direct family takes 1 <= N <= 32 only
     def call(ab, c, N):
         return lib.st24_spmm_ex(st.KERNEL_MMA_SP_DIRECT, 0, ab, c, 128, N, 256, 1.0, FAKE, FAKE, FAKE, 256, 0.0,
                                 FAKE, 128, None, None, 0, None)
 
-    assert call(st.S8, st.S32, 8) == 2
-    assert call(st.E4M3, st.BF16, 8) == 2
-    assert call(st.BF16, st.BF16, 33) == 2
+    for ab, c in ((st.BF16, st.BF16), (st.F16, st.F32), (st.E4M3, st.BF16), (st.S8, st.S32)):
+        assert call(ab, c, 33) == 2
 
 
 def test_spmm_ex_rejects_unknown_kernel_and_flags(lib):

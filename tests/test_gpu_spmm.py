@@ -121,25 +121,43 @@ DIRECT_SHAPES = [(129, 1, 128), (200, 5, 384), (300, 16, 640), (64, 32, 512), (3
                  (130, 17, 4224), (1000, 9, 8192), (77, 8, 2048)]
 
 
-@pytest.mark.parametrize("ab", ["f16", "bf16"])
+@pytest.mark.parametrize("ab", ["f16", "bf16", "e4m3", "s8"])
 @pytest.mark.parametrize("c", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("M,N,K", DIRECT_SHAPES)
 def test_direct_ragged(ab, c, M, N, K):
-    check_full(inputs.spmm_case(ab, c, M, N, K, seed=M + N + K), kernel="mma_sp_direct")
-
-
-@pytest.mark.parametrize("ab", ["f16", "bf16"])
-@pytest.mark.parametrize("N,c", [(1, "bf16"), (13, "f16"), (32, "f32")])
-def test_direct_alpha_beta_scale(ab, N, c):
-    case = inputs.spmm_case(ab, c, 257, N, 640, alpha=0.5, beta=-0.75, with_scale=True, seed=11)
+    case = inputs.spmm_case(ab, c, M, N, K, a_std=0.02 if ab == "e4m3" else 1.0, seed=M + N + K,
+                            with_scale=(ab == "s8"))
     check_full(case, kernel="mma_sp_direct")
 
 
-def test_direct_rejects_int8_and_wide_n():
-    for case in (inputs.spmm_case("s8", "s32", 128, 16, 256, seed=1), inputs.spmm_case("bf16", "bf16", 128, 33, 256)):
-        with pytest.raises(st.St24Error) as e:
-            gpu_run(case, kernel="mma_sp_direct")
-        assert e.value.status == 2
+@pytest.mark.parametrize("ab", ["f16", "bf16", "e4m3", "s8"])
+@pytest.mark.parametrize("N,c", [(1, "bf16"), (13, "f16"), (32, "f32")])
+def test_direct_alpha_beta_scale(ab, N, c):
+    case = inputs.spmm_case(ab, c, 257, N, 640, alpha=0.5, beta=-0.75, with_scale=True,
+                            a_std=0.02 if ab == "e4m3" else 1.0, seed=11)
+    check_full(case, kernel="mma_sp_direct")
+
+
+@pytest.mark.parametrize("kernel", ["mma_sp", "mma_sp_direct"])
+@pytest.mark.parametrize("N", [1, 16, 32])
+def test_int8_large_sums_exact(kernel, N):
+    """int8 -> int32 stays bit-exact when the sums need 26 bits (beyond fp32's
+    24): weights and activations all large and mostly of one sign, K = 8192."""
+    g = inputs.generator(77)
+    A = torch.randint(100, 128, (256, 8192), generator=g).to(torch.int8)
+    A[:, ::61] = -128
+    X = torch.randint(96, 128, (N, 8192), generator=g).to(torch.int8)
+    case = inputs.SpmmCase(f"int8 large sums N={N}", "s8", "s32", 256, N, 8192, 1.0, 0.0, A, X, None, None)
+    _, _, (Y,) = gpu_run(case, kernel=kernel)
+    ref = oracle_full(case)
+    assert np.abs(ref).max() > 2 ** 25
+    assert np.array_equal(decode_out(Y).astype(np.int64), ref.astype(np.int64))
+
+
+def test_direct_rejects_wide_n():
+    with pytest.raises(st.St24Error) as e:
+        gpu_run(inputs.spmm_case("bf16", "bf16", 128, 33, 256), kernel="mma_sp_direct")
+    assert e.value.status == 2
 
 
 @pytest.mark.parametrize("N", [8, 200])
