@@ -30,23 +30,26 @@ METRIC = "2:4 SpMM TFLOP/s and % of sparse tensor peak / HBM roofline on 1 GB300
 UNIT = "TFLOP/s"
 
 # Workloads: (name, element type, output type, weight shapes [(M, K)], activation widths, layers,
-#             weight std, beta, per-row scale)
+#             weight std, beta, per-row scale).  `layers` distinct weights of each shape per step,
+#             so each product is launched behind another product (as in a model's layer stack),
+#             not behind a graph boundary, and every step streams its weights from HBM.
 WORKLOADS = {
     "decode_bf16": dict(ab="bf16", c="bf16", shapes=[(4096, 4096)], Ns=list(inputs.DECODE_NS), layers=16,
                         a_std=0.02, beta=0.0, scale=False,
                         desc="decode-shaped bf16 2:4 SpMM: 16 distinct 4096x4096 weights N(0,0.02), "
                              "activations N(0,1) for N in {1,8,16,32}, bf16 out"),
-    "prefill_bf16": dict(ab="bf16", c="bf16", shapes=list(inputs.PREFILL_SHAPES), Ns=[4096], layers=1,
+    "prefill_bf16": dict(ab="bf16", c="bf16", shapes=list(inputs.PREFILL_SHAPES), Ns=[4096], layers=2,
                          a_std=0.02, beta=1.0, scale=False,
-                         desc="prefill-shaped bf16 2:4 SpMM: 11008x4096 and 4096x11008 weights, N=4096, "
-                              "beta=1 with C N(0,1), bf16 out"),
-    "int8": dict(ab="s8", c="bf16", shapes=[(8192, 8192)], Ns=list(inputs.INT8_NS), layers=1, a_std=1.0,
+                         desc="prefill-shaped bf16 2:4 SpMM: 2 x (11008x4096 and 4096x11008) distinct weights, "
+                              "N=4096, beta=1 with C N(0,1), bf16 out"),
+    "int8": dict(ab="s8", c="bf16", shapes=[(8192, 8192)], Ns=list(inputs.INT8_NS), layers=2, a_std=1.0,
                  beta=0.0, scale=True,
-                 desc="int8 2:4 SpMM: 8192x8192 weights uniform [-127,127], N in {16,2048}, int32 accumulate, "
-                      "per-row fp32 scale, bf16 out"),
-    "fp8": dict(ab="e4m3", c="bf16", shapes=[(28672, 8192)], Ns=list(inputs.FP8_NS), layers=1, a_std=0.02,
+                 desc="int8 2:4 SpMM: 2 distinct 8192x8192 weights uniform [-127,127], N in {16,2048}, "
+                      "int32 accumulate, per-row fp32 scale, bf16 out"),
+    "fp8": dict(ab="e4m3", c="bf16", shapes=[(28672, 8192)], Ns=list(inputs.FP8_NS), layers=2, a_std=0.02,
                 beta=0.0, scale=False, extra_prune_bf16=(28672, 8192),
-                desc="fp8-e4m3 2:4 SpMM: 28672x8192 weights N(0,0.02), N in {1,64,512,4096,8192}, bf16 out"),
+                desc="fp8-e4m3 2:4 SpMM: 2 distinct 28672x8192 weights N(0,0.02), N in {1,64,512,4096,8192}, "
+                     "bf16 out"),
 }
 
 
