@@ -160,6 +160,33 @@ def test_direct_rejects_wide_n():
     assert e.value.status == 2
 
 
+@pytest.mark.parametrize("kernel,ab,N", [("tcgen05", "bf16", 100), ("tcgen05", "e4m3", 300), ("mma_sp", "f16", 24),
+                                         ("mma_sp", "s8", 100), ("mma_sp_direct", "bf16", 24),
+                                         ("mma_sp_direct", "e4m3", 9)])
+@pytest.mark.parametrize("pad_c", [8, 3])
+def test_strided_b_and_c(kernel, ab, N, pad_c):
+    """B and C as views into wider buffers (ldb = K + 64, ldc = M + pad_c): the
+    product reads and writes through the strides and leaves the padding alone."""
+    M, K = 200, 512
+    c = "s32" if ab == "s8" else "bf16"
+    case = inputs.spmm_case(ab, c, M, N, K, a_std=0.02 if ab == "e4m3" else 1.0, seed=3,
+                            beta=0.0 if ab == "s8" else 0.5)
+    values, meta = st.compress(case.A.to(DEV))
+    Xw = torch.zeros((N, K + 64), dtype=case.X.dtype, device=DEV)
+    Xw[:, :K] = case.X.to(DEV)
+    tdt = inputs.TORCH_DTYPE[c]
+    Yw = torch.full((N, M + pad_c), 7, dtype=tdt, device=DEV)
+    if case.C_in is not None:
+        Yw[:, :M] = case.C_in.to(DEV).to(tdt)
+    wsz = st.st24_spmm_workspace_bytes(ab, c, M, N, K)
+    ws = torch.zeros(max(wsz, 1), dtype=torch.uint8, device=DEV)
+    st.st24_spmm(values, meta, Xw[:, :K], Yw[:, :M], K=K, beta=case.beta, workspace=ws, kernel=kernel)
+    torch.cuda.synchronize()
+    assert st.st24_device_status() == 0
+    assert bool((Yw[:, M:] == 7).all())
+    assert_close(decode_out(Yw[:, :M].contiguous()), oracle_full(case), ab, c, case.name + " strided")
+
+
 @pytest.mark.parametrize("N", [8, 200])
 def test_int8_int32_bit_exact(N):
     case = inputs.spmm_case("s8", "s32", 384, N, 1024, seed=N)
