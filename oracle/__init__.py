@@ -20,6 +20,11 @@ What each function follows (web pages, cited by title and section):
   C = alpha * (A_sparse * B) + beta * C as the product's definition.
 * ``values_bytes`` / ``meta_bytes``: the chapter's storage accounting (half
   the values plus a 2-bit index per kept value).
+* ``quantize_prune_compress`` / ``encode_e4m3``: the same chapter, section
+  "Sparsity + Quantization Combine", and "Establishing a Scalable Sparse
+  Ecosystem with the Universal Sparse Tensor Abstraction", section "Building
+  a Practical Compression Pipeline" (2:4 pruning stacked with 8-bit weights);
+  the per-row absmax arithmetic is a reading (R7 in ``st24_oracle.c``).
 
 Pins (tests/test_oracle_pins.py): the worked example, the listing's printed
 invariants and byte counts, brute force over all 6 masks of every group,
@@ -49,7 +54,7 @@ def build(force: bool = False) -> str:
     os.makedirs(os.path.dirname(_LIB), exist_ok=True)
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + ".tmp.%d" % os.getpid()
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
                                "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
@@ -70,6 +75,9 @@ def lib():
         _lib.orc_spmm_sampled.argtypes = [i, i, i64, i64, i64, d, p, p, p, i64, d, p, i64, p,
                                           p, p, i64, p, p, i]
         _lib.orc_decode.argtypes = [i, p, i64, p]
+        _lib.orc_quantize_prune_compress.argtypes = [i, i, p, i64, i64, i64, p, p, p, p]
+        _lib.orc_enc_e4m3.argtypes = [ctypes.c_float]
+        _lib.orc_enc_e4m3.restype = ctypes.c_uint8
         _lib.orc_meta_row_bytes.argtypes = [i64]
         _lib.orc_meta_row_bytes.restype = i64
         _lib.orc_values_bytes.argtypes = [i, i64, i64]
@@ -134,6 +142,35 @@ def prune_compress(dt, W: np.ndarray):
     if rc != 0:
         raise ValueError("oracle prune_compress: K must be a multiple of 4 and the type known")
     return pruned, mask, values, meta
+
+
+def quantize_prune_compress(src, dst, W: np.ndarray):
+    """Per-row quantisation of a 16-bit weight (raw storage, M x K) to e4m3 or
+    int8 (reading R7 of st24_oracle.c), then prune + compress of the codes.
+
+    Returns (codes M x K before pruning, values M x K/2, meta M x ceil(K/8)
+    uint8, scales M float32), codes and values as raw storage of ``dst``.
+    """
+    src, dst = _code(src), _code(dst)
+    W = _as_storage(src, W)
+    M, K = W.shape
+    st = _NP_STORAGE[dst]
+    codes = np.empty((M, K), st)
+    values = np.empty((M, K // 2), st)
+    meta = np.empty((M, meta_row_bytes(K)), np.uint8)
+    scales = np.empty(M, np.float32)
+    rc = lib().orc_quantize_prune_compress(src, dst, _ptr(W), M, K, K, _ptr(codes), _ptr(values), _ptr(meta),
+                                           _ptr(scales))
+    if rc != 0:
+        raise ValueError("oracle quantize_prune_compress: 16-bit source, 8-bit destination, K % 4 == 0")
+    return codes, values, meta, scales
+
+
+def encode_e4m3(x: np.ndarray) -> np.ndarray:
+    """fp32 -> e4m3 codes, nearest-even, saturated to +-448 (reading R7)."""
+    x = np.ascontiguousarray(x, np.float32).ravel()
+    f = lib().orc_enc_e4m3
+    return np.array([f(float(v)) for v in x], np.uint8)
 
 
 def decompress(dt, values: np.ndarray, meta: np.ndarray, K: int) -> np.ndarray:

@@ -42,6 +42,7 @@
  *  R5 values are row-major M x K/2 in the element type, the pair of group g
  *     at columns 2g (index i0) and 2g+1 (index i1).
  *  R6 the product sums k in ascending order; beta == 0 means C is not read.
+ *  R7 the per-row quantisation before the prune (see orc_quantize_prune_compress).
  */
 #include <math.h>
 #include <pthread.h>
@@ -197,6 +198,98 @@ int orc_prune_compress(int dt, const void* W, int64_t M, int64_t K, int64_t ldw,
             }
         }
     }
+    return 0;
+}
+
+/* ------------------------------------- quantise, then prune and compress */
+
+/*
+ * fp32 -> OCP FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits;
+ * normal values (1 + m/8) * 2^(e-7), subnormals m/8 * 2^-6, largest finite
+ * 448), rounding to nearest with ties to even, magnitudes at or above 448
+ * saturated to 448.  x must be finite.
+ */
+static uint8_t enc_e4m3_sat(float x)
+{
+    uint8_t s = signbit(x) ? 0x80 : 0;
+    double a = fabs((double)x);                /* exact */
+    if (a >= 448.0) return s | 0x7E;           /* 1.1111.110 = 448 */
+    if (a == 0.0) return s;
+    int e;
+    (void)frexp(a, &e);                        /* a in [2^(e-1), 2^e) */
+    int E = e - 1;
+    if (E < -6) {
+        /* subnormal binade: units of 2^-9; 8 units is the smallest normal */
+        double q = nearbyint(ldexp(a, 9));
+        return s | (uint8_t)q;
+    }
+    double q = nearbyint(ldexp(a, 3 - E));     /* the significand in eighths: 8..16 */
+    int mant = (int)q - 8;
+    if (mant == 8) { E += 1; mant = 0; }
+    int code = ((E + 7) << 3) | mant;
+    if (code > 0x7E) code = 0x7E;
+    return s | (uint8_t)code;
+}
+
+/* fp32 -> int8 rounding to nearest with ties to even, clamped to [-127, 127]. */
+static int8_t enc_s8_sat(float x)
+{
+    float r = nearbyintf(x);
+    if (r > 127.0f) r = 127.0f;
+    if (r < -127.0f) r = -127.0f;
+    return (int8_t)r;
+}
+
+uint8_t orc_enc_e4m3(float x) { return enc_e4m3_sat(x); }
+
+/*
+ * Per-row quantisation of a 16-bit weight followed by the prune and compress
+ * above ("Chapter 26 -- Sparsity: The Hardware View", section "Sparsity +
+ * Quantization Combine": 2:4 sparsity and 8-bit weights stack; "Establishing
+ * a Scalable Sparse Ecosystem with the Universal Sparse Tensor Abstraction",
+ * section "Building a Practical Compression Pipeline": prune plus INT8
+ * post-training quantisation).  The pages give the pipeline, not its
+ * arithmetic; reading R7:
+ *   amax  = max |w| over the row (w decoded exactly to fp32);
+ *   inv   = Q / amax in fp32 (Q = 448 for e4m3, 127 for int8);
+ *   code  = encode(fp32(w) * inv), the product rounded once to fp32, then
+ *           encoded as above (e4m3: nearest-even, saturated; int8: nearest-
+ *           even, clamped to [-127, 127]);
+ *   scale = amax / Q in fp32, so that w ~ code * scale;
+ *   a row with amax = 0 gets scale 0 and all-zero codes.
+ * The codes of the row are then pruned and compressed exactly as by
+ * orc_prune_compress (the dst type's magnitude order).  W must be finite.
+ * codes (M x K, may be NULL) receives the quantised rows before pruning.
+ * Returns 0, or -1 for an unknown type pair or K not a multiple of 4.
+ */
+int orc_quantize_prune_compress(int src, int dst, const void* W, int64_t M, int64_t K, int64_t ldw,
+                                void* codes, void* values, uint8_t* meta, float* scales)
+{
+    if ((src != ORC_F16 && src != ORC_BF16) || (dst != ORC_E4M3 && dst != ORC_S8) || K % 4 != 0) return -1;
+    const float Q = dst == ORC_E4M3 ? 448.0f : 127.0f;
+    uint8_t* row = (uint8_t*)malloc((size_t)(K > 0 ? K : 1));
+    if (!row) return -1;
+    int64_t mrb = orc_meta_row_bytes(K);
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t* wr = (const uint16_t*)W + m * ldw;
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float a = (float)fabs(load_real(src, wr, k));
+            if (a > amax) amax = a;
+        }
+        float inv = amax > 0.0f ? Q / amax : 0.0f;
+        scales[m] = amax > 0.0f ? amax / Q : 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float y = (float)load_real(src, wr, k) * inv;
+            row[k] = dst == ORC_E4M3 ? enc_e4m3_sat(y) : (uint8_t)enc_s8_sat(y);
+        }
+        if (codes) memcpy((uint8_t*)codes + m * K, row, (size_t)K);
+        int rc = orc_prune_compress(dst, row, 1, K, K, NULL, NULL,
+                                    values ? (uint8_t*)values + m * (K / 2) : NULL,
+                                    meta ? meta + m * mrb : NULL);
+        if (rc != 0) { free(row); return rc; }
+    }
+    free(row);
     return 0;
 }
 

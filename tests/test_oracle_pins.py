@@ -263,3 +263,95 @@ def test_threads_do_not_change_results():
     b, _ = oracle.spmm("f16", "f32", values, meta, bits(case.X), K, nthreads=5)
     assert np.array_equal(a, b)
     assert math.isfinite(float(a.sum()))
+
+
+# ---- quantise, then prune and compress (reading R7 of the oracle) ---------------
+
+def _torch_e4m3(x: np.ndarray) -> np.ndarray:
+    """torch's own fp32 -> float8_e4m3fn cast (nearest-even), as codes."""
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_encoder_matches_torch():
+    # every finite e4m3 value, the midpoints between neighbours (ties go to the
+    # even code), the floats next to each midpoint, and a random spread over
+    # the whole range including the subnormals
+    vals = oracle.decode("e4m3", np.arange(256, dtype=np.uint8))
+    fin = np.unique(np.abs(vals[np.isfinite(vals)])).astype(np.float64)
+    mids = (fin[:-1] + fin[1:]) / 2
+    rng = np.random.default_rng(5)
+    xs = np.concatenate([fin, mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+                         np.nextafter(mids.astype(np.float32), np.float32(1000)),
+                         rng.uniform(0, 448, 4000), np.exp2(rng.uniform(-12, 8.8, 4000))]).astype(np.float32)
+    xs = xs[np.abs(xs) <= 448]
+    xs = np.concatenate([xs, -xs])
+    assert np.array_equal(oracle.encode_e4m3(xs), _torch_e4m3(xs))
+
+
+def test_e4m3_encoder_saturates():
+    xs = np.array([448.0, 449.0, 464.0, 480.0, 1e4, 3.0e38], np.float32)
+    assert list(oracle.encode_e4m3(xs)) == [0x7E] * len(xs)
+    assert list(oracle.encode_e4m3(-xs)) == [0xFE] * len(xs)
+
+
+def test_quantize_worked_example():
+    # Row [1, -2, 3, -4, 0.5, 0.25, -0.125, 8]: amax = 8, inv = 448 / 8 = 56, so
+    # the scaled row is [56, -112, 168, -224, 28, 14, -7, 448]; in e4m3 these
+    # are 56 (1.75 * 2^5), -112, 160 (168 = 1.3125 * 2^7 is a tie between 1.25
+    # and 1.375; the even mantissa 2 wins), -224, 28, 14, -7, 448.  Group 0
+    # keeps indices 2, 3 (|160|, |224|), group 1 keeps 0, 3 (|28|, |448|).
+    W = torch.tensor([[1, -2, 3, -4, 0.5, 0.25, -0.125, 8]], dtype=torch.bfloat16)
+    codes, values, meta, scales = oracle.quantize_prune_compress("bf16", "e4m3", W.view(torch.uint16).numpy())
+    expect = _torch_e4m3(np.array([56, -112, 160, -224, 28, 14, -7, 448], np.float32))
+    assert np.array_equal(codes[0], expect)
+    assert np.array_equal(values[0], expect[[2, 3, 4, 7]])
+    assert meta[0, 0] == (2 | 3 << 2) | (0 | 3 << 2) << 4
+    assert scales[0] == np.float32(8) / np.float32(448)
+    # int8: inv = 127 / 8 = 15.875; 15.875, -31.75, 47.625, -63.5, 7.9375,
+    # 3.96875, -1.984375, 127 round (ties to even) to 16, -32, 48, -64 (a tie:
+    # -63.5 -> -64), 8, 4, -2, 127
+    codes, values, meta, scales = oracle.quantize_prune_compress("bf16", "s8", W.view(torch.uint16).numpy())
+    assert list(codes[0]) == [16, -32, 48, -64, 8, 4, -2, 127]
+    assert list(values[0]) == [48, -64, 8, 127]
+
+
+@pytest.mark.parametrize("src", ["bf16", "f16"])
+@pytest.mark.parametrize("dst", ["e4m3", "s8"])
+def test_quantize_against_numpy_and_torch(src, dst):
+    # codes recomputed independently: numpy fp32 arithmetic for amax, inv and
+    # the scaled row, torch's e4m3 cast / numpy's round-half-even for the codes;
+    # then the oracle's own prune of those codes (pinned above) must give the
+    # values and metadata
+    g = inputs.generator(9)
+    W = (torch.randn(37, 96, generator=g) * torch.exp(torch.randn(37, 1, generator=g))).to(inputs.TORCH_DTYPE[src])
+    W[5] = 0
+    raw = W.view(torch.uint16).numpy()
+    codes, values, meta, scales = oracle.quantize_prune_compress(src, dst, raw)
+    w = W.float().numpy()
+    Q = np.float32(448 if dst == "e4m3" else 127)
+    amax = np.abs(w).max(axis=1).astype(np.float32)
+    inv = np.where(amax > 0, Q / np.where(amax > 0, amax, 1), np.float32(0)).astype(np.float32)
+    y = (w * inv[:, None]).astype(np.float32)
+    if dst == "e4m3":
+        ref = _torch_e4m3(np.clip(y, -448, 448)).reshape(y.shape)
+    else:
+        ref = np.clip(np.rint(y), -127, 127).astype(np.int8)
+    assert np.array_equal(codes.view(np.uint8), ref.view(np.uint8))
+    assert np.array_equal(scales, np.where(amax > 0, amax / Q, 0).astype(np.float32))
+    assert not codes[5].any() and scales[5] == 0
+    # every non-zero row reaches the top code exactly once its absmax is scaled
+    dec = oracle.decode(dst, codes).reshape(codes.shape)
+    nz = amax > 0
+    assert np.all(np.abs(dec[nz]).max(axis=1) == float(Q))
+    _, _, v2, m2 = oracle.prune_compress(dst, codes)
+    assert np.array_equal(values.view(np.uint8), v2.view(np.uint8)) and np.array_equal(meta, m2)
+    # reconstruction error: half a step of the 8-bit grid, scaled back, plus
+    # the fp32 roundings of inv, of the scaled value and of the scale (each a
+    # relative 2^-24 of a code of at most Q: below 1e-4 of the scale)
+    err = np.abs(dec * scales[:, None] - w)
+    slack = 1e-4 * scales[:, None]
+    if dst == "s8":
+        assert np.all(err <= 0.5 * scales[:, None] + slack)
+    else:
+        step = np.maximum(np.abs(w) * 2.0 ** -4, 2.0 ** -10 * scales[:, None])
+        assert np.all(err <= step + slack)
