@@ -317,7 +317,23 @@ def run_gpu(args, w, rank, world):
         us = e0.elapsed_time(e1) / reps * 1e3
         nbytes = M * K * 2 + M * K // 2 * 2 + M * K // 8
         extra = {"shape": [M, K], "us_per_launch": us, "GB/s": nbytes / (us * 1e-6) / 1e9, "bytes": nbytes}
-        del Wb, vb, mb
+        del vb, mb
+        # the same weight quantised per row to e4m3, then pruned and compressed, in one pass
+        vq = torch.empty((M, K // 2), dtype=torch.float8_e4m3fn, device=Wb.device)
+        mq = torch.empty((M, K // 8), dtype=torch.uint8, device=Wb.device)
+        sq = torch.empty(M, dtype=torch.float32, device=Wb.device)
+        for _ in range(3):
+            st.st24_quantize_prune_compress(Wb, vq, mq, sq, stream=stream)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                st.st24_quantize_prune_compress(Wb, vq, mq, sq, stream=stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / reps * 1e3
+        nbytes = M * K * 2 + M * K // 2 + M * K // 8 + 4 * M
+        extra["quantize_e4m3"] = {"us_per_launch": us, "GB/s": nbytes / (us * 1e-6) / 1e9, "bytes": nbytes}
+        del Wb, vq, mq, sq
     total_ms = ev[0][0].elapsed_time(ev[-1][-1])
     prune_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
     spmm_ms = sum(e[1].elapsed_time(e[-1]) for e in ev)
@@ -575,7 +591,14 @@ def main():
                                  "tensor_peak_tflops": tpeak, "tensor_peak_source": tpeak_src,
                                  "groups": per_group}}}
     if r.get("extra_prune"):
-        line["kernels"]["prune_compress_bf16"] = r["extra_prune"]
+        ep = dict(r["extra_prune"])
+        q = ep.pop("quantize_e4m3", None)
+        ep["frac_hbm"] = ep["GB/s"] / hbm
+        line["kernels"]["prune_compress_bf16"] = ep
+        if q:
+            q["frac_hbm"] = q["GB/s"] / hbm
+            q["shape"] = ep["shape"]
+            line["kernels"]["quantize_prune_compress_bf16_to_e4m3"] = q
     if rank == 0 and not args.no_e2e:
         e2e_ms, h2d, d2h = run_e2e(args, w, r["layers"], r["stream"])
         line["e2e"] = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,

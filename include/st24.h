@@ -137,6 +137,37 @@ ST24_API st24_status st24_prune_compress(st24_dtype type, const void* W, int64_t
                                 void* values, void* meta, void* stream);
 
 /*
+ * Quantise, then prune and compress ([CH26] "Sparsity + Quantization
+ * Combine": 2:4 sparsity and 8-bit weights stack; "Establishing a Scalable
+ * Sparse Ecosystem with the Universal Sparse Tensor Abstraction", section
+ * "Building a Practical Compression Pipeline": prune plus INT8 post-training
+ * quantisation).  Per row m of the 16-bit weight W, in fp32 arithmetic with
+ * round-to-nearest and no contraction:
+ *   amax      = max_k |W[m][k]|,  Q = 448 (ST24_E4M3) or 127 (ST24_S8),
+ *   inv       = Q / amax,  code = encode(W[m][k] * inv),
+ *   scales[m] = amax / Q   (so W ~ code * scales[m]);
+ * encode is nearest-even with saturation to +-448 (e4m3) or nearest-even
+ * clamped to [-127, 127] (int8); a row with amax == 0 gets scales[m] = 0
+ * and zero codes.  The codes are then pruned and compressed exactly as by
+ * st24_prune_compress with type dst_type, in one pass over W (read once when
+ * K <= 16384).  Pass the result to st24_spmm with row_scale = scales (times
+ * any activation scale) to get the dequantised product.
+ *   src_type : ST24_F16 or ST24_BF16;  dst_type : ST24_E4M3 or ST24_S8.
+ *   W        : device, M x K, row stride ldw >= K; must be finite (NaN or
+ *              Inf give unspecified codes).
+ *   values   : device, st24_values_bytes(dst_type, M, K) bytes, written.
+ *   meta     : device, st24_meta_bytes(M, K) bytes, written.
+ *   scales   : device, M floats, written.
+ * K must be a multiple of 16 (else ST24_ERR_UNSUPPORTED); W and
+ * ldw*2 16-byte aligned, values 8-byte, meta 2-byte and scales 4-byte
+ * aligned (else ST24_ERR_MISALIGNED).  M == 0 is a no-op.  Bit-exact and
+ * deterministic.
+ */
+ST24_API st24_status st24_quantize_prune_compress(st24_dtype src_type, st24_dtype dst_type, const void* W,
+                                                  int64_t M, int64_t K, int64_t ldw, void* values, void* meta,
+                                                  float* scales, void* stream);
+
+/*
  * Inverse of compression ([SS24] "How Engineers Enable 2:4 Sparsity": the
  * libraries handle compression and decompression; [CH26] pruned row
  * [w0 0 0 w3 | 0 w5 w6 0]): writes the M x K dense matrix W (row stride

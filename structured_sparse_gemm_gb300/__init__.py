@@ -63,6 +63,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.st24_meta_bytes.restype = sz
     lib.st24_prune_compress.argtypes = [i, p, i64, i64, i64, p, p, p]
     lib.st24_prune_compress.restype = i
+    lib.st24_quantize_prune_compress.argtypes = [i, i, p, i64, i64, i64, p, p, p, p]
+    lib.st24_quantize_prune_compress.restype = i
     lib.st24_decompress.argtypes = [i, p, p, i64, i64, p, i64, p]
     lib.st24_decompress.restype = i
     lib.st24_spmm_workspace_bytes.argtypes = [i, i, i64, i64, i64]
@@ -133,6 +135,18 @@ def st24_prune_compress(W: torch.Tensor, values: torch.Tensor, meta: torch.Tenso
                                       _ptr(meta), _stream(stream)), "st24_prune_compress")
 
 
+def st24_quantize_prune_compress(W: torch.Tensor, values: torch.Tensor, meta: torch.Tensor, scales: torch.Tensor,
+                                 *, stream=None) -> None:
+    """Quantise each row of W [M, K] (f16/bf16) to values' 8-bit type (e4m3 or int8) with a
+    per-row absmax scale, prune the codes to 2:4 and write their compressed form and the scales."""
+    M, K = W.shape
+    if W.stride(1) != 1:
+        raise ValueError("W must have unit stride along K")
+    _check(load().st24_quantize_prune_compress(dtype_code(W.dtype), dtype_code(values.dtype), _ptr(W), M, K,
+                                               W.stride(0), _ptr(values), _ptr(meta), _ptr(scales),
+                                               _stream(stream)), "st24_quantize_prune_compress")
+
+
 def st24_decompress(values: torch.Tensor, meta: torch.Tensor, W: torch.Tensor, *, stream=None) -> None:
     """Expand a compressed form into W [M, K] (+0 at dropped positions)."""
     M, K = W.shape
@@ -201,6 +215,16 @@ def compress(W: torch.Tensor, *, stream=None):
     meta = torch.empty((M, (K // 4 + 1) // 2), dtype=torch.uint8, device=W.device)
     st24_prune_compress(W, values, meta, stream=stream)
     return values, meta
+
+
+def quantize_compress(W: torch.Tensor, dtype=torch.float8_e4m3fn, *, stream=None):
+    """(values, meta, scales) of W [M, K] quantised per row to ``dtype`` (float8_e4m3fn or int8)."""
+    M, K = W.shape
+    values = torch.empty((M, K // 2), dtype=dtype, device=W.device)
+    meta = torch.empty((M, (K // 4 + 1) // 2), dtype=torch.uint8, device=W.device)
+    scales = torch.empty(M, dtype=torch.float32, device=W.device)
+    st24_quantize_prune_compress(W, values, meta, scales, stream=stream)
+    return values, meta, scales
 
 
 class Workspace:

@@ -13,6 +13,9 @@
 // loaded before any is used, which keeps enough bytes in flight per SM.
 #include "st24_device.cuh"
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 namespace st24 {
 namespace {
 
@@ -418,6 +421,129 @@ __global__ void __launch_bounds__(kThreads) decompress_any(
 
 bool aligned(const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// ---- quantise to 8 bits, then prune and compress --------------------------
+// Per row of a 16-bit weight: amax = max |w|; inv = Q / amax and every
+// scaled value w * inv in fp32 (round to nearest, no contraction); the codes
+// are e4m3 (nearest-even, saturated to +-448) or int8 (nearest-even, clamped
+// to [-127, 127]); scale = amax / Q; a zero row gets scale 0 and zero codes.
+// ("Chapter 26 -- Sparsity: The Hardware View", section "Sparsity +
+// Quantization Combine": 2:4 sparsity and 8-bit weights stack.)  The codes
+// of each 16-value piece are then pruned and compressed like an 8-bit
+// weight's.  One CTA per row (grid-stride over rows): when the row fits in
+// registers (K <= 256 threads x 4 pieces x 16), it is read once.
+constexpr int kQPieces = 4;   // 16-value pieces per thread held in registers
+
+template <int ST>
+__device__ __forceinline__ float to_f32(uint32_t bits16) {
+  if constexpr (ST == kBF16) return __uint_as_float(bits16 << 16);
+  else return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16)));
+}
+
+// |w| of 8 16-bit values (exact).
+template <int ST>
+__device__ __forceinline__ float absmax8(const uint4 v, float m) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m = fmaxf(m, fabsf(to_f32<ST>(w[i] & 0xFFFFu)));
+    m = fmaxf(m, fabsf(to_f32<ST>(w[i] >> 16)));
+  }
+  return m;
+}
+
+// The 16 codes (byte j = value j) of a piece of 16 values given as two uint4.
+template <int ST, int DT>
+__device__ __forceinline__ uint4 quantize16(const uint4 lo, const uint4 hi, float inv) {
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t pair = w[2 * i + h];
+      const float y0 = __fmul_rn(to_f32<ST>(pair & 0xFFFFu), inv);
+      const float y1 = __fmul_rn(to_f32<ST>(pair >> 16), inv);
+      uint32_t two;
+      if constexpr (DT == kE4M3) {
+        two = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
+      } else {
+        const int q0 = min(127, max(-127, __float2int_rn(y0)));
+        const int q1 = min(127, max(-127, __float2int_rn(y1)));
+        two = (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8);
+      }
+      word |= (two & 0xFFFFu) << (16 * h);
+    }
+    out[i] = word;
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+template <int ST, int DT, bool FITS>
+__global__ void __launch_bounds__(kThreads) quantize_prune_compress_rows(
+    const uint8_t* __restrict__ W, int64_t w_row_bytes, int64_t M, int64_t K, uint8_t* __restrict__ values,
+    uint8_t* __restrict__ meta, float* __restrict__ scales) {
+  __shared__ float red[kThreads / 32];
+  const int64_t P = K / 16;   // pieces per row
+  const float Q = DT == kE4M3 ? 448.0f : 127.0f;
+  for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
+    const uint8_t* row = W + m * w_row_bytes;
+    uint4 held[FITS ? kQPieces : 1][2];
+    float amax = 0.0f;
+    if constexpr (FITS) {
+#pragma unroll
+      for (int i = 0; i < kQPieces; ++i) {
+        const int64_t pc = threadIdx.x + static_cast<int64_t>(i) * kThreads;
+        if (pc < P) {
+          held[i][0] = __ldcs(reinterpret_cast<const uint4*>(row + pc * 32));
+          held[i][1] = __ldcs(reinterpret_cast<const uint4*>(row + pc * 32 + 16));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kQPieces; ++i)
+        if (threadIdx.x + static_cast<int64_t>(i) * kThreads < P)
+          amax = absmax8<ST>(held[i][1], absmax8<ST>(held[i][0], amax));
+    } else {
+      for (int64_t pc = threadIdx.x; pc < P; pc += kThreads) {
+        const uint4 lo = __ldcg(reinterpret_cast<const uint4*>(row + pc * 32));
+        const uint4 hi = __ldcg(reinterpret_cast<const uint4*>(row + pc * 32 + 16));
+        amax = absmax8<ST>(hi, absmax8<ST>(lo, amax));
+      }
+    }
+    // the row's absolute maximum, in every thread
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kThreads / 32; ++i) amax = fmaxf(amax, red[i]);
+    const float inv = amax > 0.0f ? __fdiv_rn(Q, amax) : 0.0f;
+    if (threadIdx.x == 0) scales[m] = amax > 0.0f ? __fdiv_rn(amax, Q) : 0.0f;
+    uint8_t* vrow = values + m * (K / 2);
+    uint8_t* erow = meta + m * (K / 8);
+    auto emit = [&](int64_t pc, const uint4 lo, const uint4 hi) {
+      const uint4 codes = quantize16<ST, DT>(lo, hi, inv);
+      uint2 v;
+      uint32_t mb;
+      if (!compress_piece_lanes<DT, 1>(codes, v, mb)) v = compress_piece<DT, 1>(codes, mb);
+      *reinterpret_cast<uint2*>(vrow + pc * 8) = v;
+      *reinterpret_cast<uint16_t*>(erow + pc * 2) = static_cast<uint16_t>(mb);
+    };
+    if constexpr (FITS) {
+#pragma unroll
+      for (int i = 0; i < kQPieces; ++i) {
+        const int64_t pc = threadIdx.x + static_cast<int64_t>(i) * kThreads;
+        if (pc < P) emit(pc, held[i][0], held[i][1]);
+      }
+    } else {
+      for (int64_t pc = threadIdx.x; pc < P; pc += kThreads)
+        emit(pc, __ldcs(reinterpret_cast<const uint4*>(row + pc * 32)),
+             __ldcs(reinterpret_cast<const uint4*>(row + pc * 32 + 16)));
+    }
+    __syncthreads();   // red[] is reused by the next row
+  }
+}
+
 // Blocks that stay resident on one SM for kernel `k` (queried once per kernel).
 template <typename Kernel>
 int resident_blocks(Kernel k) {
@@ -512,6 +638,30 @@ st24_status launch_prune_compress(int dt, const void* W, int64_t M, int64_t K, i
     case kS8: launch_pc<kS8, 1>(W, M, K, ldw, values, meta, dev->num_sms, fast, stream); break;
     default: return ST24_ERR_UNSUPPORTED;
   }
+  return cudaGetLastError() == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;
+}
+
+st24_status launch_quantize_prune_compress(int src, int dst, const void* W, int64_t M, int64_t K, int64_t ldw,
+                                           void* values, void* meta, float* scales, cudaStream_t stream) {
+  const DeviceInfo* dev = current_device_info();
+  if (!dev) return ST24_ERR_CUDA;
+  const bool fits = K <= static_cast<int64_t>(kThreads) * kQPieces * 16;
+  const auto* w = static_cast<const uint8_t*>(W);
+  auto* v = static_cast<uint8_t*>(values);
+  auto* e = static_cast<uint8_t*>(meta);
+  auto go = [&](auto kern) {
+    const int64_t cap = static_cast<int64_t>(dev->num_sms) * resident_blocks(kern);
+    const int grid = static_cast<int>(M < cap ? M : cap);
+    kern<<<grid, kThreads, 0, stream>>>(w, ldw * 2, M, K, v, e, scales);
+  };
+#define ST24_QPC(S, D)                                                          \
+  if (src == S && dst == D) {                                                  \
+    if (fits) go(quantize_prune_compress_rows<S, D, true>);                    \
+    else go(quantize_prune_compress_rows<S, D, false>);                        \
+  }
+  ST24_QPC(kBF16, kE4M3) else ST24_QPC(kBF16, kS8) else ST24_QPC(kF16, kE4M3) else ST24_QPC(kF16, kS8) else
+    return ST24_ERR_UNSUPPORTED;
+#undef ST24_QPC
   return cudaGetLastError() == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;
 }
 

@@ -249,6 +249,22 @@ st24_status st24_prune_compress(st24_dtype type, const void* W, int64_t M, int64
   return launch_prune_compress(type, W, M, K, ldw, values, meta, static_cast<cudaStream_t>(stream));
 }
 
+st24_status st24_quantize_prune_compress(st24_dtype src_type, st24_dtype dst_type, const void* W, int64_t M,
+                                         int64_t K, int64_t ldw, void* values, void* meta, float* scales,
+                                         void* stream) {
+  if (M < 0 || K < 0 || K % 4 != 0) return ST24_ERR_INVALID_ARG;
+  if ((src_type != ST24_F16 && src_type != ST24_BF16) || (dst_type != ST24_E4M3 && dst_type != ST24_S8))
+    return ST24_ERR_UNSUPPORTED;
+  if (M == 0) return ST24_OK;
+  if (!scales || (K > 0 && (!W || !values || !meta || ldw < K))) return ST24_ERR_INVALID_ARG;
+  if (K % 16 != 0) return ST24_ERR_UNSUPPORTED;
+  if ((K > 0 && (!aligned(W, 16) || (ldw * 2) % 16 != 0 || !aligned(values, 8) || !aligned(meta, 2))) ||
+      !aligned(scales, 4))
+    return ST24_ERR_MISALIGNED;
+  return launch_quantize_prune_compress(src_type, dst_type, W, M, K, ldw, values, meta, scales,
+                                        static_cast<cudaStream_t>(stream));
+}
+
 st24_status st24_decompress(st24_dtype type, const void* values, const void* meta, int64_t M,
                             int64_t K, void* W, int64_t ldw, void* stream) {
   if (!is_ab_type(type) || M < 0 || K < 0 || K % 4 != 0) return ST24_ERR_INVALID_ARG;

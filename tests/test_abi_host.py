@@ -77,6 +77,19 @@ def test_prune_compress_rejects_bad_arguments(lib):
     assert lib.st24_decompress(st.E4M3, FAKE, None, 4, 8, FAKE, 8, None) == 1
 
 
+def test_quantize_prune_compress_rejects_bad_arguments(lib):
+    def call(src=st.BF16, dst=st.E4M3, W=FAKE, M=8, K=64, ldw=64, values=FAKE, meta=FAKE, scales=FAKE):
+        return lib.st24_quantize_prune_compress(src, dst, W, M, K, ldw, values, meta, scales, None)
+
+    assert call(M=-1) == 1 and call(K=6) == 1              # invalid sizes
+    assert call(src=st.F32) == 2 and call(dst=st.BF16) == 2 and call(src=st.E4M3, dst=st.S8) == 2
+    assert call(M=0) == 0                                  # nothing to do
+    assert call(W=None) == 1 and call(scales=None) == 1 and call(ldw=32) == 1
+    assert call(K=8, ldw=8) == 2                           # K % 16 != 0
+    assert call(W=FAKE + 2) == 3 and call(ldw=68) == 3 and call(values=FAKE + 4) == 3
+    assert call(meta=FAKE + 1) == 3 and call(scales=FAKE + 2) == 3
+
+
 def test_spmm_rejects_bad_arguments(lib):
     f = lib.st24_spmm
 
