@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 2) spmm_direct_kernel(const Params p
   using Sh = Shape<DT>;
   using L = Smem<DT, NT>;
   using Acc = typename std::conditional<Sh::kInt, int, float>::type;
-  constexpr int NR = L::NR;                                 // B columns staged (zero past N)
+  constexpr int NR = L::NR;                                 // B columns of the fragment layout (only n < N staged)
   // Independent accumulator chains (fewer for 8-bit inputs: four MMAs per
   // window already, and the registers go to the metadata and int sums).
   constexpr int KACC = Sh::k8 ? (NT == 1 && !Sh::kInt ? 2 : 1) : (NT == 1 ? 4 : (NT == 2 ? 2 : 1));
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 2) spmm_direct_kernel(const Params p
     for (int c = threadIdx.x; c < chunks; c += kThreads)
       if (kr + (c % 64) * (16 / ES) >= K) *reinterpret_cast<uint4*>(sBn + 16 * c) = zero;
 
-    // B into fragment order (and, for 8-bit inputs, f16).  Values (k, k+1)
+    // B into fragment order (and, for 8-bit inputs, f16), columns n < N only.  Values (k, k+1)
     // of column n at K offset kk = WK j + 4 G + e (group G of window j,
     // element e even) are MMA mp's word jj of lane t, with G split as
     // G = 2 MPW (2 h + a) + 2 mp + s:  jj = h + 2 s, t = 2 a + e / 2.
@@ -257,8 +257,6 @@ __global__ void __launch_bounds__(kThreads, 2) spmm_direct_kernel(const Params p
         sB[(((j * MPW + mp) * NR + n) * 4 + tt) * 4 + jj] = wv;
       }
     }
-    const int pad = (NR - N) * 16;   // words of the zero columns, per (window, mma)
-    for (int c = threadIdx.x; c < kWPW * MPW * pad; c += kThreads) sB[(c / pad) * NR * 16 + N * 16 + c % pad] = 0u;
     __syncthreads();
 
 #pragma unroll
@@ -307,7 +305,10 @@ __global__ void __launch_bounds__(kThreads, 2) spmm_direct_kernel(const Params p
         }
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
-          const uint4 bv = *reinterpret_cast<const uint4*>(&sB[(((j * MPW + mp) * NR + i * 8 + gid) * 4 + t) * 4]);
+          // columns past N multiply as zeros (their slots are never staged)
+          const uint4 bv = i * 8 + gid < N
+                               ? *reinterpret_cast<const uint4*>(&sB[(((j * MPW + mp) * NR + i * 8 + gid) * 4 + t) * 4])
+                               : zero;
           const uint32_t b[4] = {bv.x, bv.y, bv.z, bv.w};
           mma_sp_16832<Sh::MMA_DT>(acc[(MPW * j + mp) % KACC][i], a, b, e);
         }
