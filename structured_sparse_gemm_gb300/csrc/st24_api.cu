@@ -180,7 +180,7 @@ int resolve_kernel(int requested, const SpmmArgs& a, int num_sms) {
   if (a.ab == kE4M3) return ST24_KERNEL_TCGEN05;
   const double intensity = 2.0 * static_cast<double>(a.N) / (elem_size(a.ab) / 2.0 + 0.125);
   if (intensity > 64.0) return ST24_KERNEL_TCGEN05;
-  return direct_one_wave(a, num_sms) ? ST24_KERNEL_MMA_SP_DIRECT : ST24_KERNEL_MMA_SP;
+  return direct_applies(a) && direct_one_wave(a, num_sms) ? ST24_KERNEL_MMA_SP_DIRECT : ST24_KERNEL_MMA_SP;
 }
 
 StreamKPlan plan_for(int kernel, const SpmmArgs& a, int num_sms) {

@@ -154,6 +154,13 @@ def test_int8_large_sums_exact(kernel, N):
     assert np.array_equal(decode_out(Y).astype(np.int64), ref.astype(np.int64))
 
 
+@pytest.mark.parametrize("N", [32, 33, 36, 37])
+def test_auto_at_the_family_boundaries(N):
+    # 16-bit inputs: N <= 32 runs the register-direct kernel, 33..36 the
+    # TMA-ring one (still bound by the weights' bytes), 37 and up tcgen05
+    check_full(inputs.spmm_case("bf16", "bf16", 512, N, 1024, a_std=0.02, seed=N))
+
+
 def test_direct_rejects_wide_n():
     with pytest.raises(st.St24Error) as e:
         gpu_run(inputs.spmm_case("bf16", "bf16", 128, 33, 256), kernel="mma_sp_direct")
