@@ -25,6 +25,9 @@ What each function follows (web pages, cited by title and section):
   Ecosystem with the Universal Sparse Tensor Abstraction", section "Building
   a Practical Compression Pipeline" (2:4 pruning stacked with 8-bit weights);
   the per-row absmax arithmetic is a reading (R7 in ``st24_oracle.c``).
+* ``prune_compress_nm``: the same chapter, section "Block Sparsity, N:M
+  Generalizations, and Channel Pruning" (keep N of every M; 1:4, 2:8, ...),
+  written in the 2:4 form (reading R8).
 
 Pins (tests/test_oracle_pins.py): the worked example, the listing's printed
 invariants and byte counts, brute force over all 6 masks of every group,
@@ -76,6 +79,7 @@ def lib():
                                           p, p, i64, p, p, i]
         _lib.orc_decode.argtypes = [i, p, i64, p]
         _lib.orc_quantize_prune_compress.argtypes = [i, i, p, i64, i64, i64, p, p, p, p]
+        _lib.orc_prune_compress_nm.argtypes = [i, i, i, p, i64, i64, i64, p, p, p]
         _lib.orc_enc_e4m3.argtypes = [ctypes.c_float]
         _lib.orc_enc_e4m3.restype = ctypes.c_uint8
         _lib.orc_meta_row_bytes.argtypes = [i64]
@@ -164,6 +168,23 @@ def quantize_prune_compress(src, dst, W: np.ndarray):
     if rc != 0:
         raise ValueError("oracle quantize_prune_compress: 16-bit source, 8-bit destination, K % 4 == 0")
     return codes, values, meta, scales
+
+
+def prune_compress_nm(dt, n: int, m: int, W: np.ndarray):
+    """Keep the n largest |w| of every m consecutive elements along K (ties to the
+    lower index; reading R8 of st24_oracle.c) and write the result in the 2:4 form.
+
+    Returns (pruned M x K, values M x K/2, meta M x ceil(K/8) uint8)."""
+    dt = _code(dt)
+    W = _as_storage(dt, W)
+    M, K = W.shape
+    pruned = np.empty_like(W)
+    values = np.empty((M, K // 2), W.dtype)
+    meta = np.empty((M, meta_row_bytes(K)), np.uint8)
+    rc = lib().orc_prune_compress_nm(dt, n, m, _ptr(W), M, K, K, _ptr(pruned), _ptr(values), _ptr(meta))
+    if rc != 0:
+        raise ValueError("oracle prune_compress_nm: (n, m) in {1, 2} x {4, 8}, K % m == 0, a known type")
+    return pruned, values, meta
 
 
 def encode_e4m3(x: np.ndarray) -> np.ndarray:

@@ -43,6 +43,7 @@
  *     at columns 2g (index i0) and 2g+1 (index i1).
  *  R6 the product sums k in ascending order; beta == 0 means C is not read.
  *  R7 the per-row quantisation before the prune (see orc_quantize_prune_compress).
+ *  R8 N:M pruning written in the 2:4 form (see orc_prune_compress_nm).
  */
 #include <math.h>
 #include <pthread.h>
@@ -290,6 +291,74 @@ int orc_quantize_prune_compress(int src, int dst, const void* W, int64_t M, int6
         if (rc != 0) { free(row); return rc; }
     }
     free(row);
+    return 0;
+}
+
+/* ------------------------------------------- N:M prune into the 2:4 form */
+
+/*
+ * N:M generalisations ("Chapter 26 -- Sparsity: The Hardware View", section
+ * "Block Sparsity, N:M Generalizations, and Channel Pruning": 1:4, 2:8 and
+ * friends keep N of every M consecutive weights).  Reading R8: in every group
+ * of M consecutive elements along K keep the N of largest magnitude, ties to
+ * the lower index (the order of reading R2), chosen one at a time like
+ * select_pair.  With M = 4 or 8 and N <= 2 every aligned 4-element subgroup
+ * keeps at most 2 elements, so the result is written in the 2:4 compressed
+ * form: a subgroup with 2 kept elements stores them; with 1, the kept one
+ * and the lowest-index dropped one as a +0 partner; with none, indices 0
+ * and 1 with +0 values.  The pair is stored in ascending index order.
+ * pruned (M x K, may be NULL) receives W with every dropped element +0.
+ * Returns 0, or -1 for an unsupported (n, m), a K not a multiple of m or an
+ * unknown type.
+ */
+int orc_prune_compress_nm(int dt, int n, int m, const void* W, int64_t M, int64_t K, int64_t ldw,
+                          void* pruned, void* values, uint8_t* meta)
+{
+    int es = elem_size(dt);
+    if (es == 0 || dt == ORC_S32 || dt == ORC_F32 || (m != 4 && m != 8) || n < 1 || n > 2 || K % m != 0) return -1;
+    const uint8_t* w = (const uint8_t*)W;
+    int64_t mrb = orc_meta_row_bytes(K);
+    if (meta) memset(meta, 0, (size_t)(M * mrb));
+    for (int64_t r = 0; r < M; ++r) {
+        for (int64_t g0 = 0; g0 < K; g0 += m) {
+            double v[8];
+            int keep[8] = {0};
+            for (int j = 0; j < m; ++j) v[j] = load_real(dt, w + (r * ldw) * es, g0 + j);
+            for (int t = 0; t < n; ++t) {           /* the t-th largest: first maximum not yet kept */
+                int best = -1;
+                for (int j = 0; j < m; ++j)
+                    if (!keep[j] && (best < 0 || mag_greater(v[j], v[best]))) best = j;
+                keep[best] = 1;
+            }
+            for (int j = 0; j < m; ++j) {
+                if (!pruned) continue;
+                uint8_t* dst = (uint8_t*)pruned + (r * K + g0 + j) * es;
+                if (keep[j]) memcpy(dst, w + (r * ldw + g0 + j) * es, es);
+                else memset(dst, 0, es);
+            }
+            for (int q = 0; q < m / 4; ++q) {       /* the 4-element subgroups, in the 2:4 form */
+                int idx[2], cnt = 0;
+                for (int j = 0; j < 4 && cnt < 2; ++j)
+                    if (keep[4 * q + j]) idx[cnt++] = j;
+                int nk = cnt;
+                for (int j = 0; j < 4 && cnt < 2; ++j)    /* fill with the lowest dropped indices */
+                    if (!keep[4 * q + j] && (cnt == 0 || j != idx[0])) idx[cnt++] = j;
+                int i0 = idx[0] < idx[1] ? idx[0] : idx[1], i1 = idx[0] < idx[1] ? idx[1] : idx[0];
+                int64_t g = (g0 + 4 * q) / 4;
+                if (values) {
+                    uint8_t* vrow = (uint8_t*)values + (r * (K / 2)) * es;
+                    const int ii[2] = {i0, i1};
+                    for (int h = 0; h < 2; ++h) {
+                        uint8_t* dst = vrow + (2 * g + h) * es;
+                        if (keep[4 * q + ii[h]]) memcpy(dst, w + (r * ldw + 4 * g + ii[h]) * es, es);
+                        else memset(dst, 0, es);
+                    }
+                }
+                (void)nk;
+                if (meta) meta[r * mrb + g / 2] |= (uint8_t)((i0 | (i1 << 2)) << (4 * (g % 2)));
+            }
+        }
+    }
     return 0;
 }
 

@@ -355,3 +355,59 @@ def test_quantize_against_numpy_and_torch(src, dst):
     else:
         step = np.maximum(np.abs(w) * 2.0 ** -4, 2.0 ** -10 * scales[:, None])
         assert np.all(err <= step + slack)
+
+
+# ---- N:M prune written in the 2:4 form (reading R8 of the oracle) -----------------
+
+@pytest.mark.parametrize("n,m", [(1, 4), (1, 8), (2, 8)])
+@pytest.mark.parametrize("dt", ["bf16", "s8"])
+def test_nm_bruteforce(dt, n, m):
+    # tie-heavy rows: the kept set of every m-group maximises sum |x|, and
+    # among the maximisers it is the lexicographically smallest index set
+    rng = np.random.default_rng(n * 10 + m)
+    vals = rng.choice([-3, -2, -1, 0, 1, 2, 3], size=(64, 8 * m))
+    W = torch.tensor(vals, dtype=inputs.TORCH_DTYPE[dt])
+    pruned, values, meta = oracle.prune_compress_nm(dt, n, m, inputs.raw(W).numpy())
+    kept = oracle.decode(dt, pruned).reshape(pruned.shape) != 0
+    mags = np.abs(vals)
+    for r in range(vals.shape[0]):
+        for g0 in range(0, vals.shape[1], m):
+            grp = mags[r, g0:g0 + m]
+            best = max(itertools.combinations(range(m), n), key=lambda c: (sum(grp[list(c)]), [-i for i in c]))
+            want = np.zeros(m, bool)
+            want[list(best)] = True
+            # a kept zero decodes to 0: compare on the non-zero elements
+            assert np.array_equal(kept[r, g0:g0 + m], want & (grp != 0))
+
+
+@pytest.mark.parametrize("n,m", [(1, 4), (1, 8), (2, 8)])
+@pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3", "s8"])
+def test_nm_structure_and_roundtrip(dt, n, m):
+    g = inputs.generator(n + m)
+    W = inputs.draw(dt, (33, 16 * m), 0.02 if dt == "e4m3" else 1.0, g)
+    raw = inputs.raw(W).numpy()
+    pruned, values, meta = oracle.prune_compress_nm(dt, n, m, raw)
+    dec = oracle.decode(dt, pruned).reshape(pruned.shape)
+    # exactly n non-zeros in every m-group (no zeros in these inputs' kept slots)
+    nz = (dec != 0).reshape(dec.shape[0], -1, m).sum(axis=2)
+    assert np.all(nz <= n) and np.mean(nz == n) > 0.99
+    # every 4-subgroup holds at most 2: the 2:4 form decompresses to the pruned matrix
+    assert np.array_equal(oracle.decompress(dt, values, meta, 16 * m).view(np.uint8), pruned.view(np.uint8))
+    # the pruned matrix keeps exactly the kept elements of W
+    same = (pruned.view(np.uint8).reshape(dec.shape + (-1,)) == raw.view(np.uint8).reshape(dec.shape + (-1,))).all(-1)
+    assert np.all(same | (dec == 0))
+
+
+def test_nm_two_of_four_is_the_plain_prune():
+    W = inputs.draw("bf16", (17, 64), 1.0, inputs.generator(3))
+    raw = inputs.raw(W).numpy()
+    p1, v1, m1 = oracle.prune_compress_nm("bf16", 2, 4, raw)
+    p2, _, v2, m2 = oracle.prune_compress("bf16", raw)
+    assert np.array_equal(p1, p2) and np.array_equal(v1, v2) and np.array_equal(m1, m2)
+
+
+def test_nm_rejects_unsupported():
+    raw = np.zeros((2, 16), np.uint16)
+    for n, m in ((3, 8), (0, 4), (2, 16), (1, 3)):
+        with pytest.raises(ValueError):
+            oracle.prune_compress_nm("bf16", n, m, raw)
