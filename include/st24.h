@@ -137,6 +137,25 @@ ST24_API st24_status st24_prune_compress(st24_dtype type, const void* W, int64_t
                                 void* values, void* meta, void* stream);
 
 /*
+ * N:M prune and compress into the 2:4 form ([CH26] "Block Sparsity, N:M
+ * Generalizations, and Channel Pruning": keep N of every M consecutive
+ * weights; 1:4, 2:8, ...).  In every group of m consecutive elements along K
+ * the n of largest magnitude are kept (magnitude and ties as for
+ * st24_prune_compress).  Supported: n in {1, 2}, m in {4, 8} (else
+ * ST24_ERR_UNSUPPORTED); every aligned 4-element subgroup then keeps at most
+ * two, so the output is the compressed form of st24_prune_compress (same
+ * sizes and layout): a subgroup with one kept element stores it with a +0
+ * partner at its lowest dropped index, one with none stores +0 at indices 0
+ * and 1.  st24_spmm multiplies it exactly; st24_decompress gives the N:M
+ * pruned matrix.  (2, 4) is st24_prune_compress.  K must be a multiple of 4
+ * and of m; W aligned to the element size and values to twice it (else
+ * ST24_ERR_MISALIGNED).  M or K == 0 is a no-op.  Bit-exact and
+ * deterministic.
+ */
+ST24_API st24_status st24_prune_compress_nm(st24_dtype type, int n, int m, const void* W, int64_t M, int64_t K,
+                                            int64_t ldw, void* values, void* meta, void* stream);
+
+/*
  * Quantise, then prune and compress ([CH26] "Sparsity + Quantization
  * Combine": 2:4 sparsity and 8-bit weights stack; "Establishing a Scalable
  * Sparse Ecosystem with the Universal Sparse Tensor Abstraction", section

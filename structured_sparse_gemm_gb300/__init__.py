@@ -63,6 +63,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.st24_meta_bytes.restype = sz
     lib.st24_prune_compress.argtypes = [i, p, i64, i64, i64, p, p, p]
     lib.st24_prune_compress.restype = i
+    lib.st24_prune_compress_nm.argtypes = [i, i, i, p, i64, i64, i64, p, p, p]
+    lib.st24_prune_compress_nm.restype = i
     lib.st24_quantize_prune_compress.argtypes = [i, i, p, i64, i64, i64, p, p, p, p]
     lib.st24_quantize_prune_compress.restype = i
     lib.st24_decompress.argtypes = [i, p, p, i64, i64, p, i64, p]
@@ -133,6 +135,17 @@ def st24_prune_compress(W: torch.Tensor, values: torch.Tensor, meta: torch.Tenso
         raise ValueError("W must have unit stride along K")
     _check(load().st24_prune_compress(dtype_code(W.dtype), _ptr(W), M, K, W.stride(0), _ptr(values),
                                       _ptr(meta), _stream(stream)), "st24_prune_compress")
+
+
+def st24_prune_compress_nm(W: torch.Tensor, values: torch.Tensor, meta: torch.Tensor, n: int, m: int, *,
+                           stream=None) -> None:
+    """Keep the n largest-|w| of every m consecutive elements of W [M, K] along K ((n, m) in
+    {1, 2} x {4, 8}) and write the result in the 2:4 compressed form."""
+    M, K = W.shape
+    if W.stride(1) != 1:
+        raise ValueError("W must have unit stride along K")
+    _check(load().st24_prune_compress_nm(dtype_code(W.dtype), n, m, _ptr(W), M, K, W.stride(0), _ptr(values),
+                                         _ptr(meta), _stream(stream)), "st24_prune_compress_nm")
 
 
 def st24_quantize_prune_compress(W: torch.Tensor, values: torch.Tensor, meta: torch.Tensor, scales: torch.Tensor,
@@ -214,6 +227,15 @@ def compress(W: torch.Tensor, *, stream=None):
     values = torch.empty((M, K // 2), dtype=W.dtype, device=W.device)
     meta = torch.empty((M, (K // 4 + 1) // 2), dtype=torch.uint8, device=W.device)
     st24_prune_compress(W, values, meta, stream=stream)
+    return values, meta
+
+
+def compress_nm(W: torch.Tensor, n: int, m: int, *, stream=None):
+    """(values, meta) of W [M, K] pruned n:m, in the 2:4 compressed form."""
+    M, K = W.shape
+    values = torch.empty((M, K // 2), dtype=W.dtype, device=W.device)
+    meta = torch.empty((M, (K // 4 + 1) // 2), dtype=torch.uint8, device=W.device)
+    st24_prune_compress_nm(W, values, meta, n, m, stream=stream)
     return values, meta
 
 

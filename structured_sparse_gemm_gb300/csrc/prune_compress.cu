@@ -421,6 +421,89 @@ __global__ void __launch_bounds__(kThreads) decompress_any(
 
 bool aligned(const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// ---- N:M prune into the 2:4 form -----------------------------------------
+// ("Chapter 26 -- Sparsity: The Hardware View", section "Block Sparsity, N:M
+// Generalizations, and Channel Pruning": keep N of every M consecutive
+// weights.)  In every group of m elements along K the n of largest
+// magnitude are kept (the order of mag_key; ties to the lower index).  With
+// m = 4 or 8 and n <= 2 each aligned 4-element subgroup keeps at most two,
+// so the result is a 2:4 compressed form (+0 partners at the lowest dropped
+// indices) that st24_spmm multiplies exactly.  One thread per 8 elements of
+// a row (two subgroups: one metadata byte); neighbouring threads take
+// neighbouring elements, so the warp's loads and stores are contiguous.
+template <int DT, int ES>
+__global__ void __launch_bounds__(kThreads) prune_compress_nm_kernel(const uint8_t* __restrict__ W, int64_t w_row_bytes,
+                                                                     int64_t M, int64_t K, int n, int m,
+                                                                     uint8_t* __restrict__ values,
+                                                                     uint8_t* __restrict__ meta, int vec) {
+  const int64_t upr = (K + 7) / 8;   // 8-element units per row
+  const int64_t total = M * upr;
+  const int64_t mrb = meta_row_bytes(K);
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < total;
+       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = u / upr, c0 = (u - r * upr) * 8;
+    const int cnt = K - c0 < 8 ? static_cast<int>(K - c0) : 8;   // 4 or 8
+    const uint8_t* src = W + r * w_row_bytes + c0 * ES;
+    uint32_t e[8], k[8];
+    if (vec && cnt == 8) {
+      // the unit in one load (16-byte aligned rows of 16-bit values, 8-byte of 8-bit ones)
+      uint32_t w[4];
+      if constexpr (ES == 2) {
+        const uint4 v = __ldcs(reinterpret_cast<const uint4*>(src));
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) e[j] = (w[j / 2] >> (16 * (j & 1))) & 0xFFFFu;
+      } else {
+        const uint2 v = __ldcs(reinterpret_cast<const uint2*>(src));
+        w[0] = v.x; w[1] = v.y;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) e[j] = (w[j / 4] >> (8 * (j & 3))) & 0xFFu;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        e[j] = 0u;
+        if (j < cnt) e[j] = ES == 2 ? static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(src)[j]) : src[j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) k[j] = mag_key<DT>(e[j]);
+    bool keep[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int b = (j / m) * m;   // this element's m-group inside the unit
+      int above = 0;               // elements of the group that outrank it
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i >= b && i < b + m && i != j && (k[i] > k[j] || (k[i] == k[j] && i < j))) ++above;
+      keep[j] = j < cnt && above < n;
+    }
+    uint32_t mb = 0;
+    uint8_t* vrow = values + r * (K / 2) * ES;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      if (4 * q >= cnt) break;
+      int idx[2] = {0, 0}, c = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (keep[4 * q + j] && c < 2) idx[c++] = j;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (!keep[4 * q + j] && c < 2 && (c == 0 || j != idx[0])) idx[c++] = j;
+      const int i0 = idx[0] < idx[1] ? idx[0] : idx[1], i1 = idx[0] < idx[1] ? idx[1] : idx[0];
+      const uint32_t v0 = keep[4 * q + i0] ? e[4 * q + i0] : 0u, v1 = keep[4 * q + i1] ? e[4 * q + i1] : 0u;
+      const int64_t col = c0 / 2 + 2 * q;   // value column of the pair
+      if constexpr (ES == 2) {
+        *reinterpret_cast<uint32_t*>(vrow + col * 2) = v0 | (v1 << 16);
+      } else {
+        *reinterpret_cast<uint16_t*>(vrow + col) = static_cast<uint16_t>(v0 | (v1 << 8));
+      }
+      mb |= static_cast<uint32_t>(i0 | (i1 << 2)) << (4 * q);
+    }
+    meta[r * mrb + c0 / 8] = static_cast<uint8_t>(mb);
+  }
+}
+
 // ---- quantise to 8 bits, then prune and compress --------------------------
 // Per row of a 16-bit weight: amax = max |w|; inv = Q / amax and every
 // scaled value w * inv in fp32 (round to nearest, no contraction); the codes
@@ -636,6 +719,28 @@ st24_status launch_prune_compress(int dt, const void* W, int64_t M, int64_t K, i
     case kBF16: launch_pc<kBF16, 2>(W, M, K, ldw, values, meta, dev->num_sms, fast, stream); break;
     case kE4M3: launch_pc<kE4M3, 1>(W, M, K, ldw, values, meta, dev->num_sms, fast, stream); break;
     case kS8: launch_pc<kS8, 1>(W, M, K, ldw, values, meta, dev->num_sms, fast, stream); break;
+    default: return ST24_ERR_UNSUPPORTED;
+  }
+  return cudaGetLastError() == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;
+}
+
+st24_status launch_prune_compress_nm(int dt, int n, int m, const void* W, int64_t M, int64_t K, int64_t ldw,
+                                     void* values, void* meta, cudaStream_t stream) {
+  const DeviceInfo* dev = current_device_info();
+  if (!dev) return ST24_ERR_CUDA;
+  const int64_t units = M * ((K + 7) / 8);
+  auto go = [&](auto kern, int es) {
+    const int va = 8 * es;   // bytes of one unit: its vector load needs this alignment
+    const int vec = aligned(W, va) && (ldw * es) % va == 0 ? 1 : 0;
+    kern<<<grid_for(kern, units, kThreads, dev->num_sms), kThreads, 0, stream>>>(
+        static_cast<const uint8_t*>(W), ldw * es, M, K, n, m, static_cast<uint8_t*>(values),
+        static_cast<uint8_t*>(meta), vec);
+  };
+  switch (dt) {
+    case kF16: go(prune_compress_nm_kernel<kF16, 2>, 2); break;
+    case kBF16: go(prune_compress_nm_kernel<kBF16, 2>, 2); break;
+    case kE4M3: go(prune_compress_nm_kernel<kE4M3, 1>, 1); break;
+    case kS8: go(prune_compress_nm_kernel<kS8, 1>, 1); break;
     default: return ST24_ERR_UNSUPPORTED;
   }
   return cudaGetLastError() == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;

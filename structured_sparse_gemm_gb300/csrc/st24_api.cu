@@ -249,6 +249,18 @@ st24_status st24_prune_compress(st24_dtype type, const void* W, int64_t M, int64
   return launch_prune_compress(type, W, M, K, ldw, values, meta, static_cast<cudaStream_t>(stream));
 }
 
+st24_status st24_prune_compress_nm(st24_dtype type, int n, int m, const void* W, int64_t M, int64_t K, int64_t ldw,
+                                   void* values, void* meta, void* stream) {
+  if (!is_ab_type(type) || M < 0 || K < 0 || K % 4 != 0) return ST24_ERR_INVALID_ARG;
+  if ((m != 4 && m != 8) || n < 1 || n > 2) return ST24_ERR_UNSUPPORTED;
+  if (K % m != 0) return ST24_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return ST24_OK;
+  if (!W || !values || !meta || ldw < K) return ST24_ERR_INVALID_ARG;
+  const int es = elem_size(type);
+  if (!aligned(W, es) || !aligned(values, 2 * es)) return ST24_ERR_MISALIGNED;
+  return launch_prune_compress_nm(type, n, m, W, M, K, ldw, values, meta, static_cast<cudaStream_t>(stream));
+}
+
 st24_status st24_quantize_prune_compress(st24_dtype src_type, st24_dtype dst_type, const void* W, int64_t M,
                                          int64_t K, int64_t ldw, void* values, void* meta, float* scales,
                                          void* stream) {

@@ -41,6 +41,8 @@ const DeviceInfo* current_device_info();
 // ---------------------------------------------------------- prune / compress
 st24_status launch_prune_compress(int dt, const void* W, int64_t M, int64_t K, int64_t ldw,
                                   void* values, void* meta, cudaStream_t stream);
+st24_status launch_prune_compress_nm(int dt, int n, int m, const void* W, int64_t M, int64_t K, int64_t ldw,
+                                     void* values, void* meta, cudaStream_t stream);
 st24_status launch_quantize_prune_compress(int src, int dst, const void* W, int64_t M, int64_t K, int64_t ldw,
                                            void* values, void* meta, float* scales, cudaStream_t stream);
 st24_status launch_decompress(int dt, const void* values, const void* meta, int64_t M, int64_t K,

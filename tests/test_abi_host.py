@@ -77,6 +77,18 @@ def test_prune_compress_rejects_bad_arguments(lib):
     assert lib.st24_decompress(st.E4M3, FAKE, None, 4, 8, FAKE, 8, None) == 1
 
 
+def test_prune_compress_nm_rejects_bad_arguments(lib):
+    def call(t=st.BF16, n=1, m=4, W=FAKE, M=8, K=64, ldw=64, values=FAKE, meta=FAKE):
+        return lib.st24_prune_compress_nm(t, n, m, W, M, K, ldw, values, meta, None)
+
+    assert call(t=st.F32) == 1 and call(K=6) == 1 and call(M=-1) == 1
+    assert call(n=3, m=8) == 2 and call(m=16) == 2 and call(n=0) == 2
+    assert call(m=8, K=12, ldw=12) == 1                   # K % m
+    assert call(M=0) == 0
+    assert call(W=None) == 1 and call(ldw=32) == 1
+    assert call(W=FAKE + 1) == 3 and call(values=FAKE + 2) == 3
+
+
 def test_quantize_prune_compress_rejects_bad_arguments(lib):
     def call(src=st.BF16, dst=st.E4M3, W=FAKE, M=8, K=64, ldw=64, values=FAKE, meta=FAKE, scales=FAKE):
         return lib.st24_quantize_prune_compress(src, dst, W, M, K, ldw, values, meta, scales, None)
