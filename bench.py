@@ -118,6 +118,20 @@ def measured_traffic(workload: str, kernel: str):
     return rec["dram_bytes_per_launch"] if rec.get("source_sha256") == kernel_source_hash() else None
 
 
+def max_over_ranks(value: float, world: int, device="cuda") -> float:
+    """The largest of every rank's value: the job's step time is its slowest replica's."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_replica_step: float, ms_step: float) -> float:
+    """Whole-job throughput: every replica's work over the slowest replica's step time."""
+    return world * flops_per_replica_step / (ms_step * 1e-3) / 1e12
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -541,13 +555,9 @@ def main():
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl")
     r = run_gpu(args, w, rank, world)
-    ms_step = r["total_ms"] / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(r["total_ms"] / args.steps, world, "cuda")
     flops = flops_per_step(w)
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = job_tflops(world, flops, ms_step)
     hbm, bf16_peak, bf16_sus, peak_kind = peaks()
 
     spmm_launch_ms = r["spmm_ms"] / args.steps / n_spmm(w)
