@@ -77,6 +77,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.st24_spmm_ex.restype = i
     lib.st24_spmm_noalloc.argtypes = [i, i, i64, i64, i64, f, p, p, p, i64, f, p, i64, p, p]
     lib.st24_spmm_noalloc.restype = i
+    lib.st24_selftest_wait_timeout.argtypes = [p]
+    lib.st24_selftest_wait_timeout.restype = i
     lib.st24_device_status.argtypes = [p]
     lib.st24_device_status.restype = i
     _lib = lib
@@ -213,6 +215,12 @@ def st24_spmm_noalloc(values: torch.Tensor, meta: torch.Tensor, X: torch.Tensor,
     _check(load().st24_spmm_noalloc(dtype_code(X.dtype), dtype_code(Y.dtype), M, N, K, float(alpha), _ptr(values),
                                     _ptr(meta), _ptr(X), X.stride(0), float(beta), _ptr(Y), Y.stride(0),
                                     _ptr(row_scale), _stream(stream)), "st24_spmm_noalloc")
+
+
+def st24_selftest_wait_timeout(*, stream=None) -> None:
+    """Enqueue the self-test whose bounded wait runs out (about a second); the next
+    st24_device_status() returns ST24_ERR_TIMEOUT (5)."""
+    _check(load().st24_selftest_wait_timeout(_stream(stream)), "st24_selftest_wait_timeout")
 
 
 def st24_device_status(stream=None) -> int:

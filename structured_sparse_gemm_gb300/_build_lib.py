@@ -16,6 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libst24.so")
+# The failure-detection self-test (linked into the library, declared in st24_selftest.h).
+SELFTEST_SRC = os.path.join(CSRC, "selftest", "st24_selftest.cu")
 # The tensor-pipe ceiling probe bench.py's roofline uses (not part of the C ABI).
 PEAK_SRC = os.path.join(CSRC, "peak", "peak_mma_sp.cu")
 PEAK_LIB = os.path.join(OUT, "libst24_peak.so")
@@ -30,9 +32,9 @@ def _nvcc() -> str:
 
 
 def _inputs():
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu"))) + [SELFTEST_SRC]
     deps = srcs + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + \
-        [os.path.join(ROOT, "include", "st24.h"), os.path.abspath(__file__)]
+        glob.glob(os.path.join(ROOT, "include", "*.h")) + [os.path.abspath(__file__)]
     return srcs, deps
 
 
