@@ -84,9 +84,12 @@ typedef enum st24_kernel {
                                  for int8; TCGEN05 otherwise (always for e4m3) */
     ST24_KERNEL_TCGEN05 = 1,  /* tcgen05.mma.sp with TMEM accumulators (f16, bf16, e4m3 only) */
     ST24_KERNEL_MMA_SP = 2,   /* warp-level mma.sp fed by a TMA ring in shared memory (all input types) */
-    ST24_KERNEL_MMA_SP_DIRECT = 3  /* warp-level mma.sp with the weights loaded straight into registers
+    ST24_KERNEL_MMA_SP_DIRECT = 3, /* warp-level mma.sp with the weights loaded straight into registers
                                       (1 <= N <= 32 only; 8-bit inputs widened exactly to f16; no
                                       workspace) */
+    ST24_KERNEL_TCGEN05_NARROW = 4 /* tcgen05.mma.sp for narrow products (1 <= N <= 64; f16, bf16, e4m3):
+                                      balanced stream-K over one CTA per SM, sized so that the next
+                                      product's CTAs fit beside it */
 } st24_kernel;
 
 /* Option bits for st24_spmm_ex (OR them together; 0 = none). */
@@ -243,8 +246,9 @@ ST24_API st24_status st24_spmm(st24_dtype ab_type, st24_dtype c_type, int64_t M,
 /*
  * st24_spmm with options: an explicitly chosen kernel family (for testing one
  * family against another, or a family against the oracle) and `flags`, a set
- * of st24_spmm_flags bits.  ST24_KERNEL_TCGEN05 with ab_type ST24_S8, and
- * ST24_KERNEL_MMA_SP_DIRECT with N > 32, return ST24_ERR_UNSUPPORTED.  Arguments, workspace and results are as for
+ * of st24_spmm_flags bits.  ST24_KERNEL_TCGEN05 or ST24_KERNEL_TCGEN05_NARROW
+ * with ab_type ST24_S8, ST24_KERNEL_MMA_SP_DIRECT with N > 32 and
+ * ST24_KERNEL_TCGEN05_NARROW with N > 64 return ST24_ERR_UNSUPPORTED.  Arguments, workspace and results are as for
  * st24_spmm (which is st24_spmm_ex with ST24_KERNEL_AUTO and no flags);
  * st24_spmm_workspace_bytes covers every family.  An unknown `kernel` or an
  * unknown flag bit returns ST24_ERR_INVALID_ARG.

@@ -25,10 +25,10 @@ __all__ = [
 ]
 
 F16, BF16, E4M3, S8, F32, S32 = 0, 1, 2, 3, 4, 5
-KERNEL_AUTO, KERNEL_TCGEN05, KERNEL_MMA_SP, KERNEL_MMA_SP_DIRECT = 0, 1, 2, 3
+KERNEL_AUTO, KERNEL_TCGEN05, KERNEL_MMA_SP, KERNEL_MMA_SP_DIRECT, KERNEL_TCGEN05_NARROW = 0, 1, 2, 3, 4
 SPMM_FIXED_A = 1   # st24_spmm_flags: A is fixed weights no in-flight work on the stream writes
 _KERNELS = {"auto": KERNEL_AUTO, "tcgen05": KERNEL_TCGEN05, "mma_sp": KERNEL_MMA_SP,
-            "mma_sp_direct": KERNEL_MMA_SP_DIRECT}
+            "mma_sp_direct": KERNEL_MMA_SP_DIRECT, "tcgen05_narrow": KERNEL_TCGEN05_NARROW}
 _TORCH_CODE = {
     torch.float16: F16, torch.bfloat16: BF16, torch.float8_e4m3fn: E4M3, torch.int8: S8,
     torch.float32: F32, torch.int32: S32,
@@ -181,8 +181,8 @@ def st24_spmm(values: torch.Tensor, meta: torch.Tensor, X: torch.Tensor, Y: torc
               kernel: str | int = "auto", fixed_a: bool = False) -> None:
     """Y[N, M] = alpha * row_scale * (A_sparse @ X.T).T + beta * Y, A given by (values, meta).
 
-    ``kernel`` picks the kernel family ("auto", "tcgen05", "mma_sp" or
-    "mma_sp_direct");
+    ``kernel`` picks the kernel family ("auto", "tcgen05", "mma_sp",
+    "mma_sp_direct" or "tcgen05_narrow");
     ``fixed_a`` declares (values, meta) fixed weights that no work still in
     flight on the stream writes (ST24_SPMM_FIXED_A).  Anything but the
     defaults goes through st24_spmm_ex."""

@@ -185,6 +185,7 @@ int resolve_kernel(int requested, const SpmmArgs& a, int num_sms) {
 
 StreamKPlan plan_for(int kernel, const SpmmArgs& a, int num_sms) {
   if (kernel == ST24_KERNEL_MMA_SP_DIRECT) return StreamKPlan{};   // one launch shape, no workspace
+  if (kernel == ST24_KERNEL_TCGEN05_NARROW) return plan_spmm_nt(a, num_sms);
   return kernel == ST24_KERNEL_TCGEN05 ? plan_spmm_tc(a, num_sms) : plan_spmm_mmasp(a, num_sms);
 }
 
@@ -302,6 +303,10 @@ size_t st24_spmm_workspace_bytes(st24_dtype ab_type, st24_dtype c_type, int64_t 
   if (ab_type != ST24_S8) {
     const size_t t = plan_spmm_tc(a, dev->num_sms).ws_bytes;
     ws = t > ws ? t : ws;
+    if (narrow_applies(a)) {
+      const size_t n = plan_spmm_nt(a, dev->num_sms).ws_bytes;
+      ws = n > ws ? n : ws;
+    }
   }
   return ws;
 }
@@ -311,7 +316,7 @@ st24_status st24_spmm_ex(st24_kernel kernel, unsigned flags, st24_dtype ab_type,
                          int64_t ldb, float beta, void* C, int64_t ldc, const float* row_scale,
                          void* workspace, size_t ws_bytes, void* stream) {
   if (kernel != ST24_KERNEL_AUTO && kernel != ST24_KERNEL_TCGEN05 && kernel != ST24_KERNEL_MMA_SP &&
-      kernel != ST24_KERNEL_MMA_SP_DIRECT)
+      kernel != ST24_KERNEL_MMA_SP_DIRECT && kernel != ST24_KERNEL_TCGEN05_NARROW)
     return ST24_ERR_INVALID_ARG;
   if (flags & ~static_cast<unsigned>(ST24_SPMM_FIXED_A)) return ST24_ERR_INVALID_ARG;
   SpmmArgs a{};
@@ -336,6 +341,7 @@ st24_status st24_spmm_ex(st24_kernel kernel, unsigned flags, st24_dtype ab_type,
   if (st != ST24_OK || M == 0 || N == 0) return st;
   if (kernel == ST24_KERNEL_TCGEN05 && ab_type == ST24_S8) return ST24_ERR_UNSUPPORTED;
   if (kernel == ST24_KERNEL_MMA_SP_DIRECT && !direct_applies(a)) return ST24_ERR_UNSUPPORTED;
+  if (kernel == ST24_KERNEL_TCGEN05_NARROW && !narrow_applies(a)) return ST24_ERR_UNSUPPORTED;
   const DeviceInfo* dev = current_device_info();
   if (!dev) return ST24_ERR_CUDA;
   const int k = resolve_kernel(kernel, a, dev->num_sms);
@@ -345,6 +351,7 @@ st24_status st24_spmm_ex(st24_kernel kernel, unsigned flags, st24_dtype ab_type,
   const StreamKPlan plan = plan_for(k, a, dev->num_sms);
   if (plan.ws_bytes > 0 && (!workspace || ws_bytes < plan.ws_bytes || !aligned(workspace, 16)))
     return ST24_ERR_WORKSPACE;
+  if (k == ST24_KERNEL_TCGEN05_NARROW) return launch_spmm_nt(a, plan, *dev, s);
   return k == ST24_KERNEL_TCGEN05 ? launch_spmm_tc(a, plan, *dev, s) : launch_spmm_mmasp(a, plan, *dev, s);
 }
 

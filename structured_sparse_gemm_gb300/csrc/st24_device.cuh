@@ -174,6 +174,14 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, 
                : "memory");
 }
 
+// The same for a 3-D tensor map.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -459,6 +467,14 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // cp.async of 16 bytes, global -> shared, cached in L2 only.
 __device__ __forceinline__ void cp_async_cg16(void* sdst, const void* gsrc) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sdst)), "l"(gsrc) : "memory");
+}
+// atomicAdd with acquire-release semantics at GPU scope: orders this thread's
+// (and, through a preceding barrier, its CTA's) earlier writes before the add,
+// and later reads after it.
+__device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }

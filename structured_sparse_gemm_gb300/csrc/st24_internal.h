@@ -106,6 +106,13 @@ bool direct_applies(const SpmmArgs& a);
 bool direct_one_wave(const SpmmArgs& a, int num_sms);
 st24_status launch_spmm_direct(const SpmmArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
+// The narrow-N tcgen05 path (N <= 64; f16, bf16, e4m3): balanced stream-K,
+// two CTAs per SM so consecutive products overlap.
+bool narrow_applies(const SpmmArgs& a);
+StreamKPlan plan_spmm_nt(const SpmmArgs& a, int num_sms);
+st24_status launch_spmm_nt(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev,
+                           cudaStream_t stream);
+
 // The tcgen05 (5th-generation tensor core) path: f16, bf16, e4m3.
 StreamKPlan plan_spmm_tc(const SpmmArgs& a, int num_sms);
 st24_status launch_spmm_tc(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev,

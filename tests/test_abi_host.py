@@ -133,12 +133,23 @@ def test_direct_kernel_rejects_what_it_does_not_cover(lib):
         assert call(ab, c, 33) == 2
 
 
+def test_narrow_kernel_rejects_what_it_does_not_cover(lib):
+    # the narrow tcgen05 family takes 1 <= N <= 64 and no int8 (no int8 tcgen05 kind on sm_103a)
+    def call(ab, c, N):
+        return lib.st24_spmm_ex(st.KERNEL_TCGEN05_NARROW, 0, ab, c, 128, N, 256, 1.0, FAKE, FAKE, FAKE, 256, 0.0,
+                                FAKE, 128, None, None, 0, None)
+
+    for ab, c in ((st.BF16, st.BF16), (st.F16, st.F32), (st.E4M3, st.BF16)):
+        assert call(ab, c, 65) == 2
+    assert call(st.S8, st.S32, 16) == 2
+
+
 def test_spmm_ex_rejects_unknown_kernel_and_flags(lib):
     def call(kernel=0, flags=0):
         return lib.st24_spmm_ex(kernel, flags, st.BF16, st.BF16, 128, 8, 256, 1.0, FAKE, FAKE, FAKE, 256, 0.0,
                                 FAKE, 128, None, None, 0, None)
 
-    assert call(kernel=4) == 1
+    assert call(kernel=5) == 1
     assert call(kernel=-1) == 1
     assert call(flags=2) == 1
     assert call(flags=1 << 31) == 1
