@@ -79,17 +79,20 @@ typedef enum st24_status {
 
 /* Kernel families st24_spmm_ex can be asked to use. */
 typedef enum st24_kernel {
-    ST24_KERNEL_AUTO = 0,     /* what st24_spmm uses: for 16-bit inputs with N <= 32 (HBM-bound)
-                                 MMA_SP_DIRECT when its grid fits in one wave, else MMA_SP; MMA_SP
-                                 for int8; TCGEN05 otherwise (always for e4m3) */
+    ST24_KERNEL_AUTO = 0,     /* what st24_spmm uses: MMA_SP for int8; for N <= 64 (bound by the
+                                 weights' bytes) TCGEN05_NARROW -- MMA_SP_DIRECT for 16-bit inputs
+                                 with N <= 4 whose grid fits in one wave; e4m3 with K not a multiple
+                                 of 256 on TCGEN05 -- and TCGEN05 for wider products */
     ST24_KERNEL_TCGEN05 = 1,  /* tcgen05.mma.sp with TMEM accumulators (f16, bf16, e4m3 only) */
     ST24_KERNEL_MMA_SP = 2,   /* warp-level mma.sp fed by a TMA ring in shared memory (all input types) */
     ST24_KERNEL_MMA_SP_DIRECT = 3, /* warp-level mma.sp with the weights loaded straight into registers
                                       (1 <= N <= 32 only; 8-bit inputs widened exactly to f16; no
                                       workspace) */
-    ST24_KERNEL_TCGEN05_NARROW = 4 /* tcgen05.mma.sp for narrow products (1 <= N <= 64; f16, bf16, e4m3):
-                                      balanced stream-K over one CTA per SM, sized so that the next
-                                      product's CTAs fit beside it */
+    ST24_KERNEL_TCGEN05_NARROW = 4 /* tcgen05.mma.sp for narrow products (1 <= N <= 64; f16, bf16, and
+                                      e4m3 with K % 256 == 0): each 128-row tile's K range split over a
+                                      cluster of up to 8 CTAs that sum their partials in distributed
+                                      shared memory; half an SM per CTA, so the next product's CTAs fit
+                                      beside it; no workspace */
 } st24_kernel;
 
 /* Option bits for st24_spmm_ex (OR them together; 0 = none). */
@@ -207,8 +210,10 @@ ST24_API st24_status st24_decompress(st24_dtype type, const void* values, const 
  * split-K / stream-K schedule and one 32-bit counter per output tile.
  * It must be zero-filled before its first use; every successful st24_spmm
  * leaves the counters at zero again, so a workspace can be reused by later
- * calls on the same stream without clearing.  Calls that run at the same
- * time must not share a workspace.
+ * calls on the same stream without clearing.  After a call whose kernels gave
+ * up on a wait (st24_device_status returns ST24_ERR_TIMEOUT) some counters
+ * may be left nonzero: zero-fill the workspace again before reusing it.
+ * Calls that run at the same time must not share a workspace.
  */
 ST24_API size_t st24_spmm_workspace_bytes(st24_dtype ab_type, st24_dtype c_type, int64_t M, int64_t N,
                                  int64_t K);

@@ -16,9 +16,10 @@ bool narrow_applies(const SpmmArgs& a) {
 }
 
 // Each 128-row tile's K range split evenly over a cluster of S CTAs: the
-// smallest S (a power of two, at most 8 and at most the tile's k-blocks) that
-// puts CTAs on about 80% of the SMs or more.  Two CTAs fit on an SM, so the
-// next product's CTAs find room beside this one's.  No workspace.
+// largest S (a power of two, at most 8 and at most the tile's k-blocks) that
+// keeps the grid within ~1.7 CTAs per SM (measured on GB300: 4096-row
+// weights run best on 8 CTAs per tile, 11008-row ones on 2, 28672-row ones
+// unsplit).  No workspace.
 StreamKPlan plan_spmm_nt(const SpmmArgs& a, int num_sms) {
   StreamKPlan pl{};
   pl.bm = 128;
@@ -29,7 +30,7 @@ StreamKPlan plan_spmm_nt(const SpmmArgs& a, int num_sms) {
   // k-block is the stage of the configuration S selects.
   const int64_t fine_iters = (a.K + nt::stage_k(elem_size(a.ab), pl.bn, true) - 1) / nt::stage_k(elem_size(a.ab), pl.bn, true);
   int S = 1;
-  while (S < 8 && 2 * S <= fine_iters && pl.tiles_m * S * 5 < 4 * static_cast<int64_t>(num_sms)) S *= 2;
+  while (S < 8 && 2 * S <= fine_iters && pl.tiles_m * 2 * S * 10 <= 17 * static_cast<int64_t>(num_sms)) S *= 2;
   pl.bk = nt::stage_k(elem_size(a.ab), pl.bn, S > 1);
   pl.k_iters = (a.K + pl.bk - 1) / pl.bk;
   pl.cluster = S;

@@ -159,28 +159,25 @@ using namespace st24;
 
 namespace {
 
-// The kernel family a call runs on: tcgen05 for the 16-bit and fp8 inputs,
-// the warp-level sparse MMA for int8 (there is no int8 tcgen05 kind on sm_103a).
 // Which kernel family st24_spmm uses (measured on GB300):
-//  * int8: the warp-level kernel (there is no int8 tcgen05 kind on sm_103a).
-//  * fp8: tcgen05 always; the warp-level e4m3 sparse MMA runs at ~1/50 of the
-//    16-bit one on this GPU.
-//  * 16-bit: while the product is bound by streaming the compressed A from
-//    HBM (2N flops per logical weight over 1.125 bytes, at most 64 flop/B:
-//    N <= 32), a warp-level kernel: the one that loads the weights straight
-//    into registers when its grid fits in one wave (the least fixed latency
-//    per launch; measured faster than the TMA-ring one at every decode width
-//    of a 4096 x 4096 weight), else the TMA-ring one, whose persistent grid
-//    pipelines across tiles; tcgen05 beyond.  (For 8-bit inputs the
-//    register-direct kernel measured slower than the families above, so it
-//    is used only when asked for.)
+//  * int8: the warp-level kernels (there is no int8 tcgen05 kind on sm_103a):
+//    the TMA-ring one (the register-direct one measured slower on the int8
+//    workload's shapes).
+//  * narrow products (N <= 64; for e4m3 with K a multiple of 256), bound by
+//    streaming the compressed weights: the narrow tcgen05 kernel -- except
+//    16-bit inputs with N <= 4 whose grid fits in one wave, where the
+//    register-direct kernel's shorter chain wins by a little.  Left over:
+//    the TMA-ring kernel (e4m3 with other K: tcgen05; the warp-level e4m3
+//    sparse MMA runs at ~1/50 of the 16-bit rate).
+//  * wider products: tcgen05 (CTA pairs for N > 64).
 int resolve_kernel(int requested, const SpmmArgs& a, int num_sms) {
   if (requested != ST24_KERNEL_AUTO) return requested;
   if (a.ab == kS8) return ST24_KERNEL_MMA_SP;
-  if (a.ab == kE4M3) return ST24_KERNEL_TCGEN05;
-  const double intensity = 2.0 * static_cast<double>(a.N) / (elem_size(a.ab) / 2.0 + 0.125);
-  if (intensity > 64.0) return ST24_KERNEL_TCGEN05;
-  return direct_applies(a) && direct_one_wave(a, num_sms) ? ST24_KERNEL_MMA_SP_DIRECT : ST24_KERNEL_MMA_SP;
+  if (a.N > 64) return ST24_KERNEL_TCGEN05;
+  const bool k16 = a.ab == kF16 || a.ab == kBF16;
+  if (k16 && a.N <= 4 && direct_applies(a) && direct_one_wave(a, num_sms)) return ST24_KERNEL_MMA_SP_DIRECT;
+  if (narrow_applies(a)) return ST24_KERNEL_TCGEN05_NARROW;
+  return k16 ? ST24_KERNEL_MMA_SP : ST24_KERNEL_TCGEN05;
 }
 
 StreamKPlan plan_for(int kernel, const SpmmArgs& a, int num_sms) {

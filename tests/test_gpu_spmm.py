@@ -154,11 +154,13 @@ def test_int8_large_sums_exact(kernel, N):
     assert np.array_equal(decode_out(Y).astype(np.int64), ref.astype(np.int64))
 
 
-@pytest.mark.parametrize("N", [32, 33, 36, 37])
-def test_auto_at_the_family_boundaries(N):
-    # 16-bit inputs: N <= 32 runs the register-direct kernel, 33..36 the
-    # TMA-ring one (still bound by the weights' bytes), 37 and up tcgen05
-    check_full(inputs.spmm_case("bf16", "bf16", 512, N, 1024, a_std=0.02, seed=N))
+@pytest.mark.parametrize("ab,N,K", [("bf16", 4, 1024), ("bf16", 5, 1024), ("bf16", 64, 1024), ("bf16", 65, 1024),
+                                    ("e4m3", 64, 1024), ("e4m3", 64, 1152), ("e4m3", 65, 1024), ("f16", 1, 1024)])
+def test_auto_at_the_family_boundaries(ab, N, K):
+    # 16-bit inputs: N <= 4 runs the register-direct kernel (one wave), 5..64
+    # the narrow tcgen05 one, 65 and up the wide tcgen05 one; e4m3 with N <= 64
+    # runs the narrow one when K is a multiple of 256, else the wide one
+    check_full(inputs.spmm_case(ab, "bf16", 512, N, K, a_std=0.02, seed=N))
 
 
 def test_direct_rejects_wide_n():
@@ -212,11 +214,12 @@ def test_k_equals_zero():
 
 
 def test_deterministic_and_workspace_reuse():
+    # the one-CTA tcgen05 kernel splits decode tiles over K through the workspace
     case = inputs.decode_bf16(32)
     wsz = st.st24_spmm_workspace_bytes("bf16", "bf16", case.M, case.N, case.K)
-    assert wsz > 0   # decode shapes are split over K
+    assert wsz > 0
     ws = torch.zeros(wsz, dtype=torch.uint8, device=DEV)
-    _, _, outs = gpu_run(case, repeat=3, ws=ws)
+    _, _, outs = gpu_run(case, repeat=3, ws=ws, kernel="tcgen05")
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
     # the per-tile counters (the workspace's last bytes) are back at zero after each call
     assert int(ws[-256:].sum()) == 0
