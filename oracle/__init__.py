@@ -28,6 +28,10 @@ What each function follows (web pages, cited by title and section):
 * ``prune_compress_nm``: the same chapter, section "Block Sparsity, N:M
   Generalizations, and Channel Pruning" (keep N of every M; 1:4, 2:8, ...),
   written in the 2:4 form (reading R8).
+* ``spmm_t`` / ``spmm_t_sampled``: the transposed use of a compressed weight,
+  dX = dY * W (the same chapter, section "2:4: ~2x on the Matmul, Less
+  End-to-End": retraining after the prune needs the layer's input gradient),
+  summed along M in ascending order (reading R9).
 
 Pins (tests/test_oracle_pins.py): the worked example, the listing's printed
 invariants and byte counts, brute force over all 6 masks of every group,
@@ -78,6 +82,8 @@ def lib():
         _lib.orc_spmm_sampled.argtypes = [i, i, i64, i64, i64, d, p, p, p, i64, d, p, i64, p,
                                           p, p, i64, p, p, i]
         _lib.orc_decode.argtypes = [i, p, i64, p]
+        _lib.orc_spmm_t.argtypes = [i, i, i64, i64, i64, d, p, p, p, i64, d, p, i64, p, p, i]
+        _lib.orc_spmm_t_sampled.argtypes = [i, i, i64, i64, i64, d, p, p, p, i64, d, p, i64, p, p, i64, p, p, i]
         _lib.orc_quantize_prune_compress.argtypes = [i, i, p, i64, i64, i64, p, p, p, p]
         _lib.orc_prune_compress_nm.argtypes = [i, i, i, p, i64, i64, i64, p, p, p]
         _lib.orc_enc_e4m3.argtypes = [ctypes.c_float]
@@ -275,6 +281,47 @@ def spmm_sampled(dt_ab, dt_c, values, meta, B, K, rows, cols, alpha=1.0, beta=0.
                                 _ptr(cols), rows.size, _ptr(out), _ptr(acc), nthreads)
     if rc < 0:
         raise ValueError("oracle spmm_sampled: bad arguments")
+    return out, acc
+
+
+def spmm_t(dt_ab, dt_c, values, meta, dY, K, alpha=1.0, beta=0.0, C_in=None, nthreads=0):
+    """dX = alpha * (dY @ A) + beta * C_in for A (M x K) in the compressed form.
+
+    dY is [N, M] (element (m, n) of the transposed product's right operand at
+    dY[n, m]); C_in and the result are dX[N, K].  Returns (out float64 [N, K],
+    acc int64 [N, K] -- the exact integer sums for int8, else zeros)."""
+    dt_ab, dt_c = _code(dt_ab), _code(dt_c)
+    values = _as_storage(dt_ab, values)
+    dY = _as_storage(dt_ab, dY)
+    meta = np.ascontiguousarray(meta, np.uint8)
+    M, N = values.shape[0], dY.shape[0]
+    C_in, ldc = _c_args(dt_c, C_in, beta)
+    out = np.empty((N, K), np.float64)
+    acc = np.zeros((N, K), np.int64)
+    rc = lib().orc_spmm_t(dt_ab, dt_c, M, N, K, alpha, _ptr(values), _ptr(meta), _ptr(dY), dY.shape[1],
+                          beta, _ptr(C_in), ldc, _ptr(out), _ptr(acc), nthreads)
+    if rc < 0:
+        raise ValueError("oracle spmm_t: bad arguments")
+    return out, acc
+
+
+def spmm_t_sampled(dt_ab, dt_c, values, meta, dY, K, ks, ns, alpha=1.0, beta=0.0, C_in=None, nthreads=0):
+    """Outputs (ks[s], ns[s]) of the transposed product, one by one."""
+    dt_ab, dt_c = _code(dt_ab), _code(dt_c)
+    values = _as_storage(dt_ab, values)
+    dY = _as_storage(dt_ab, dY)
+    meta = np.ascontiguousarray(meta, np.uint8)
+    M, N = values.shape[0], dY.shape[0]
+    ks = np.ascontiguousarray(ks, np.int64)
+    ns = np.ascontiguousarray(ns, np.int64)
+    C_in, ldc = _c_args(dt_c, C_in, beta)
+    out = np.empty(ks.shape, np.float64)
+    acc = np.zeros(ks.shape, np.int64)
+    rc = lib().orc_spmm_t_sampled(dt_ab, dt_c, M, N, K, alpha, _ptr(values), _ptr(meta), _ptr(dY), dY.shape[1],
+                                  beta, _ptr(C_in), ldc, _ptr(ks), _ptr(ns), ks.size, _ptr(out), _ptr(acc),
+                                  nthreads)
+    if rc < 0:
+        raise ValueError("oracle spmm_t_sampled: bad arguments")
     return out, acc
 
 

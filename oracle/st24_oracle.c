@@ -44,6 +44,7 @@
  *  R6 the product sums k in ascending order; beta == 0 means C is not read.
  *  R7 the per-row quantisation before the prune (see orc_quantize_prune_compress).
  *  R8 N:M pruning written in the 2:4 form (see orc_prune_compress_nm).
+ *  R9 the transposed product sums m in ascending order (see orc_spmm_t).
  */
 #include <math.h>
 #include <pthread.h>
@@ -429,6 +430,77 @@ typedef struct {
     int64_t begin, end;
 } job_t;
 
+/* ------------------------------------------- transposed use (dX = dY * W) */
+
+/*
+ * The transposed product of a compressed weight ("Chapter 26 -- Sparsity:
+ * The Hardware View", section "2:4: ~2x on the Matmul, Less End-to-End":
+ * train dense, prune to 2:4, retrain -- retraining needs the input gradient
+ * dX = dY * W of a layer Y = X * W^T).  For A (M x K) in the compressed form,
+ *   out(k, n) = alpha * sum over m ascending of A(m, k) * B(m, n)
+ *               + beta * C_in(k, n)        (fp64; int64 sums for int8),
+ * where A(m, k) is the stored value whose in-group index names k (the first
+ * of the pair if i0 names it, the second if i1 does), else 0; B(m, n) is at
+ * B[n*ldb + m] (a row-major dY[N, M]); C_in(k, n) and out(k, n) are at
+ * [n*ldc + k] and out[n*K + k] (row-major dX[N, K]).  The sum runs along M,
+ * along which the weight has no 2:4 structure.
+ */
+static void a_elem(const job_t* j, int64_t m, int64_t k, double* af, int64_t* ai)
+{
+    int64_t mrb = (j->K / 4 + 1) / 2;
+    int64_t g = k / 4;
+    int p = (int)(k % 4);
+    uint8_t nib = (j->meta[m * mrb + g / 2] >> (4 * (g % 2))) & 0xf;
+    int i0 = nib & 3, i1 = nib >> 2;
+    int64_t idx = -1;
+    if (p == i0) idx = m * (j->K / 2) + 2 * g;
+    else if (p == i1) idx = m * (j->K / 2) + 2 * g + 1;
+    if (idx < 0) { *af = 0.0; *ai = 0; return; }
+    if (j->dt_ab == ORC_S8) { *ai = ((const int8_t*)j->values)[idx]; *af = (double)*ai; }
+    else { *af = load_real(j->dt_ab, j->values, idx); *ai = 0; }
+}
+
+static double transposed_elem(const job_t* j, int64_t k, int64_t n, int64_t* acc_i)
+{
+    double sf = 0.0;
+    int64_t si = 0;
+    for (int64_t m = 0; m < j->M; ++m) {
+        double af;
+        int64_t ai;
+        a_elem(j, m, k, &af, &ai);
+        if (j->dt_ab == ORC_S8) si += ai * (int64_t)((const int8_t*)j->B)[n * j->ldb + m];
+        else sf += af * load_real(j->dt_ab, j->B, n * j->ldb + m);
+    }
+    *acc_i = si;
+    double acc = (j->dt_ab == ORC_S8) ? (double)si : sf;
+    double r = j->alpha * acc;
+    if (j->beta != 0.0) r += j->beta * load_real(j->dt_c, j->C_in, n * j->ldc + k);
+    return r;
+}
+
+static void* run_rows_t(void* arg)
+{
+    job_t* j = (job_t*)arg;
+    for (int64_t k = j->begin; k < j->end; ++k)
+        for (int64_t n = 0; n < j->N; ++n) {
+            int64_t ai;
+            j->out[n * j->K + k] = transposed_elem(j, k, n, &ai);
+            if (j->acc_i64) j->acc_i64[n * j->K + k] = ai;
+        }
+    return NULL;
+}
+
+static void* run_samples_t(void* arg)
+{
+    job_t* j = (job_t*)arg;
+    for (int64_t s = j->begin; s < j->end; ++s) {
+        int64_t ai;
+        j->out[s] = transposed_elem(j, j->rows[s], j->cols[s], &ai);
+        if (j->acc_i64) j->acc_i64[s] = ai;
+    }
+    return NULL;
+}
+
 static double epilogue(const job_t* j, int64_t m, int64_t n, double acc)
 {
     double s = j->scale ? (double)j->scale[m] : 1.0;
@@ -590,6 +662,42 @@ int orc_spmm_sampled(int dt_ab, int dt_c, int64_t M, int64_t N, int64_t K, doubl
     j.scale = scale; j.out = out; j.acc_i64 = acc_i64;
     j.rows = rows; j.cols = cols; j.nsamples = nsamples;
     return parallel_for(&j, nsamples, nthreads, run_samples);
+}
+
+static int parallel_for(job_t* base, int64_t total, int nthreads, void* (*fn)(void*));
+static int check_types(int dt_ab, int dt_c);
+
+/* The transposed product (see above), all K x N outputs; out and acc_i64 are
+ * N*K, (k, n) at [n*K + k].  Returns the threads used, or -1 on bad arguments. */
+int orc_spmm_t(int dt_ab, int dt_c, int64_t M, int64_t N, int64_t K, double alpha,
+               const void* values, const uint8_t* meta, const void* B, int64_t ldb,
+               double beta, const void* C_in, int64_t ldc, double* out, int64_t* acc_i64, int nthreads)
+{
+    if (K % 4 != 0 || check_types(dt_ab, dt_c)) return -1;
+    job_t j;
+    memset(&j, 0, sizeof j);
+    j.dt_ab = dt_ab; j.dt_c = dt_c; j.M = M; j.N = N; j.K = K; j.ldb = ldb; j.ldc = ldc;
+    j.alpha = alpha; j.beta = beta; j.values = values; j.meta = meta; j.B = B; j.C_in = C_in;
+    j.out = out; j.acc_i64 = acc_i64;
+    return parallel_for(&j, K, nthreads, run_rows_t);
+}
+
+/* Selected outputs (ks[s], ns[s]) of the transposed product; out[s]. */
+int orc_spmm_t_sampled(int dt_ab, int dt_c, int64_t M, int64_t N, int64_t K, double alpha,
+                       const void* values, const uint8_t* meta, const void* B, int64_t ldb,
+                       double beta, const void* C_in, int64_t ldc, const int64_t* ks, const int64_t* ns,
+                       int64_t nsamples, double* out, int64_t* acc_i64, int nthreads)
+{
+    if (K % 4 != 0 || check_types(dt_ab, dt_c)) return -1;
+    for (int64_t s = 0; s < nsamples; ++s)
+        if (ks[s] < 0 || ks[s] >= K || ns[s] < 0 || ns[s] >= N) return -1;
+    job_t j;
+    memset(&j, 0, sizeof j);
+    j.dt_ab = dt_ab; j.dt_c = dt_c; j.M = M; j.N = N; j.K = K; j.ldb = ldb; j.ldc = ldc;
+    j.alpha = alpha; j.beta = beta; j.values = values; j.meta = meta; j.B = B; j.C_in = C_in;
+    j.out = out; j.acc_i64 = acc_i64;
+    j.rows = ks; j.cols = ns; j.nsamples = nsamples;
+    return parallel_for(&j, nsamples, nthreads, run_samples_t);
 }
 
 /* Threads a call with nthreads = 0 would use (for reporting). */

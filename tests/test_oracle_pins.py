@@ -411,3 +411,73 @@ def test_nm_rejects_unsupported():
     for n, m in ((3, 8), (0, 4), (2, 16), (1, 3)):
         with pytest.raises(ValueError):
             oracle.prune_compress_nm("bf16", n, m, raw)
+
+
+# ---- the transposed use dX = dY * W (reading R9 of the oracle) -------------------
+
+def _small_int_case(dt, M, K, N, seed):
+    """Weights and dY with small integer values (exact in every type and in fp64 sums)."""
+    g = inputs.generator(seed)
+    if dt == "s8":
+        A = torch.randint(-9, 10, (M, K), generator=g).to(torch.int8)
+        dY = torch.randint(-9, 10, (N, M), generator=g).to(torch.int8)
+    else:
+        A = torch.randint(-9, 10, (M, K), generator=g).to(torch.float32).to(inputs.TORCH_DTYPE[dt])
+        dY = torch.randint(-9, 10, (N, M), generator=g).to(torch.float32).to(inputs.TORCH_DTYPE[dt])
+    return bits(A), bits(dY)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3", "s8"])
+def test_transposed_adjoint_of_the_forward_product(dt):
+    """<y, A x> == <A^T y, x> exactly: the transposed product is the adjoint of the
+    forward one (an index slip, a swapped i0/i1 or a transposed operand breaks it)."""
+    M, K = 48, 64
+    A, _ = _small_int_case(dt, M, K, 1, 3)
+    _, _, values, meta = oracle.prune_compress(dt, A)
+    g = inputs.generator(11)
+    for _ in range(3):
+        if dt == "s8":
+            x = torch.randint(-5, 6, (1, K), generator=g).to(torch.int8)
+            y = torch.randint(-5, 6, (1, M), generator=g).to(torch.int8)
+        else:
+            x = torch.randint(-5, 6, (1, K), generator=g).to(torch.float32).to(inputs.TORCH_DTYPE[dt])
+            y = torch.randint(-5, 6, (1, M), generator=g).to(torch.float32).to(inputs.TORCH_DTYPE[dt])
+        Ax, _ = oracle.spmm(dt, "f32", values, meta, bits(x), K)          # [1, M]
+        Aty, _ = oracle.spmm_t(dt, "f32", values, meta, bits(y), K)       # [1, K]
+        lhs = float(oracle.decode(dt, bits(y))[0] @ Ax[0])
+        rhs = float(Aty[0] @ oracle.decode(dt, bits(x))[0])
+        assert lhs == rhs
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "s8"])
+def test_transposed_equals_matmul_of_the_decompressed_weight(dt):
+    M, K, N = 40, 96, 12
+    case = inputs.spmm_case(dt, "f32", M, N, K, a_std=0.5, seed=8)
+    g = inputs.generator(21)
+    dY = inputs.draw(dt, (N, M), 1.0, g)
+    _, _, values, meta = oracle.prune_compress(dt, bits(case.A))
+    out, acc = oracle.spmm_t(dt, "f32", values, meta, bits(dY), K)
+    dense = oracle.decompress(dt, values, meta, K)                       # [M, K]
+    if dt == "s8":
+        ref = bits(dY).astype(np.int64) @ dense.astype(np.int64)          # [N, K]
+        assert np.array_equal(acc, ref)
+        assert np.array_equal(out, ref.astype(np.float64))
+    else:
+        ref = oracle.decode(dt, bits(dY)) @ oracle.decode(dt, dense)
+        assert np.allclose(out, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def test_transposed_epilogue_and_sampling():
+    M, K, N = 32, 64, 8
+    A, dY = _small_int_case("bf16", M, K, N, 5)
+    _, _, values, meta = oracle.prune_compress("bf16", A)
+    acc, _ = oracle.spmm_t("bf16", "f32", values, meta, dY, K)
+    g = inputs.generator(6)
+    cin = inputs.draw("bf16", (N, K), 1.0, g)
+    out, _ = oracle.spmm_t("bf16", "bf16", values, meta, dY, K, alpha=0.5, beta=-2.0, C_in=bits(cin))
+    assert np.array_equal(out, 0.5 * acc - 2.0 * cin.to(torch.float64).numpy())
+    rng = np.random.default_rng(1)
+    ks, ns = rng.integers(0, K, 40), rng.integers(0, N, 40)
+    samp, _ = oracle.spmm_t_sampled("bf16", "bf16", values, meta, dY, K, ks, ns, alpha=0.5, beta=-2.0,
+                                    C_in=bits(cin))
+    assert np.array_equal(samp, out[ns, ks])
