@@ -66,9 +66,15 @@ WORKLOADS = {
                       scale=False, unstructured_context=0.75,
                       desc="the listing's 4096^3 demo in bf16: 2:4 SpMM of 8 distinct 4096x4096 weights, "
                            "N=4096, beside dense and 75%-unstructured-zero dense matmuls"),
+    # The transposed use of the compressed weights dX = dY * W (retraining after the prune), at the
+    # prefill shapes: a dense contraction over M read from the compressed form (tensor-bound).
+    "transposed_bf16": dict(ab="bf16", c="bf16", shapes=list(inputs.PREFILL_SHAPES), Ns=[4096], layers=2,
+                            a_std=0.02, beta=0.0, scale=False, op="spmm_t",
+                            desc="transposed use dX = dY * W of 2 x (11008x4096 and 4096x11008) compressed bf16 "
+                                 "weights, dY of N=4096 rows, bf16 out"),
 }
 HEADLINE = "fp8"
-SUB_WORKLOADS = ["decode_bf16", "prefill_bf16", "int8", "demo_bf16"]
+SUB_WORKLOADS = ["decode_bf16", "prefill_bf16", "int8", "demo_bf16", "transposed_bf16"]
 
 
 def flops_per_pass(w):
@@ -91,9 +97,12 @@ def groups(w):
 
 
 def launch_bytes(w, M, K, N):
-    """Algorithmic HBM bytes of one product: compressed A and metadata, B, C (read too when beta != 0), scale."""
+    """Algorithmic HBM bytes of one product: compressed A and metadata, B, C (read too when beta != 0), scale.
+    For the transposed use: compressed A, dY (N x M) and dX (N x K)."""
     es = inputs.ELEM_SIZE[w["ab"]]
     cs = inputs.ELEM_SIZE[w["c"]]
+    if w.get("op") == "spmm_t":
+        return M * K // 2 * es + M * K // 8 + M * N * es + K * N * cs * (2 if w["beta"] else 1)
     return M * K // 2 * es + M * K // 8 + K * N * es + M * N * cs * (2 if w["beta"] else 1) + \
         (4 * M if w["scale"] else 0)
 
@@ -179,7 +188,7 @@ def mma_sp_peak_tops(kind: int) -> float | None:
 _MMA_SP_PEAK = {}
 
 
-def tensor_peak(ab: str, bf16_dense: float, bf16_sustained: float, long_region: bool):
+def tensor_peak(ab: str, bf16_dense: float, bf16_sustained: float, long_region: bool, dense_op: bool = False):
     """2:4-sparse tensor peak (dense-equivalent TFLOP/s) of an element type, and where it comes from.
 
     16-bit: twice the measured dense bf16 peak; e4m3: twice that again (the nominal
@@ -188,6 +197,8 @@ def tensor_peak(ab: str, bf16_dense: float, bf16_sustained: float, long_region: 
     sustained dense figure; a short one with the burst figure."""
     dense = bf16_sustained if long_region else bf16_dense
     which = "bf16_tflops_sustained" if long_region else "bf16_tflops"
+    if dense_op:   # a dense contraction (the transposed use of the compressed weight)
+        return dense, f"measured dense bf16 (MEASURED_PEAKS.json {which}): a dense MMA"
     if ab in ("bf16", "f16"):
         return 2.0 * dense, f"2 x measured dense bf16 (MEASURED_PEAKS.json {which})"
     if ab == "e4m3":
@@ -282,11 +293,13 @@ def build_workload(w, dev, seed=0):
             meta = torch.empty((M, K // 8), dtype=torch.uint8, device=dev)
             scale = inputs.row_scale(M, g).to(dev) if w["scale"] else None
             acts = []
+            t = w.get("op") == "spmm_t"
             for N in w["Ns"]:
-                X = inputs.draw(w["ab"], (N, K), 1.0, g).to(dev)
-                Y = inputs.draw(w["c"], (N, M), 1.0, g).to(dev) if w["beta"] else \
-                    torch.empty((N, M), dtype=inputs.TORCH_DTYPE[w["c"]], device=dev)
-                ws_bytes = st.st24_spmm_workspace_bytes(w["ab"], w["c"], M, N, K)
+                # X is the product's right operand ([N, K]; dY [N, M] for the transposed use), Y its output
+                X = inputs.draw(w["ab"], (N, M if t else K), 1.0, g).to(dev)
+                Y = inputs.draw(w["c"], (N, K if t else M), 1.0, g).to(dev) if w["beta"] else \
+                    torch.empty((N, K if t else M), dtype=inputs.TORCH_DTYPE[w["c"]], device=dev)
+                ws_bytes = 0 if t else st.st24_spmm_workspace_bytes(w["ab"], w["c"], M, N, K)
                 ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
                 acts.append((X, Y, ws))
             layers.append(dict(A=A, values=values, meta=meta, scale=scale, acts=acts, M=M, K=K, si=si))
@@ -299,18 +312,26 @@ def prune_phase(layers, stream=None):
         st.st24_prune_compress(L["A"], L["values"], L["meta"], stream=stream)
 
 
+def product(w, L, X, Y, ws, stream=None, kernel="auto", fixed_a=True):
+    """One product of the workload through the public API: st24_spmm, or st24_spmm_t for the transposed use."""
+    import structured_sparse_gemm_gb300 as st
+    if w.get("op") == "spmm_t":
+        st.st24_spmm_t(L["values"], L["meta"], X, Y, K=L["K"], beta=w["beta"], stream=stream)
+    else:
+        st.st24_spmm(L["values"], L["meta"], X, Y, K=L["K"], beta=w["beta"], row_scale=L["scale"],
+                     workspace=ws, stream=stream, kernel=kernel, fixed_a=fixed_a)
+
+
 def spmm_phase(layers, w, stream=None, kernel="auto", only=None, fixed_a=True):
     """The products of one pass.  Run inside a captured graph, after the prune
     graph has completed, so the weights are fixed for the whole phase
     (ST24_SPMM_FIXED_A)."""
-    import structured_sparse_gemm_gb300 as st
     for ni in range(len(w["Ns"])):
         for L in layers:
             if only is not None and (ni, L["si"]) != only:
                 continue
             X, Y, ws = L["acts"][ni]
-            st.st24_spmm(L["values"], L["meta"], X, Y, K=L["K"], beta=w["beta"], row_scale=L["scale"],
-                         workspace=ws, stream=stream, kernel=kernel, fixed_a=fixed_a)
+            product(w, L, X, Y, ws, stream=stream, kernel=kernel, fixed_a=fixed_a)
 
 
 def time_launches(fn, stream, reps=10, warm=3):
@@ -483,8 +504,7 @@ def run_e2e(args, w, layers, stream):
                     # The weights pruned by the kernel just before the first
                     # product may still be in flight: that product waits.
                     fixed = args.fixed_a and not (ni == 0 and li == 0 and len(layers) == 1)
-                    st.st24_spmm(L["values"], L["meta"], X, Y, K=L["K"], beta=w["beta"], row_scale=L["scale"],
-                                 workspace=ws, fixed_a=fixed)
+                    product(w, L, X, Y, ws, fixed_a=fixed)
             products_done.record(stream)
             for L, (hA, hX) in zip(layers, host):
                 for (X, Y, ws), (hx, hy) in zip(L["acts"], hX):
@@ -529,6 +549,10 @@ def dense_context(w, dev, zero_fraction: float = 0.0, reps: int = 20):
     fraction of unstructured zeros, multiplied by the same dense kernel.  Per group: microseconds per
     product, or the error the op raised for that shape."""
     dt, fn, label, out_dt = _dense_op(w["ab"], dev)
+    transposed = w.get("op") == "spmm_t"
+    if transposed:   # dX = dY @ W: W [M, K] is the right operand as stored
+        fn = lambda X, W, out: torch.matmul(X, W, out=out)   # noqa: E731
+        label = "torch.matmul bf16 (dY @ W)"
     res = {"op": label, "groups": []}
     total_us = 0.0
     complete = True
@@ -541,9 +565,9 @@ def dense_context(w, dev, zero_fraction: float = 0.0, reps: int = 20):
             Ws.append(W.to(dt) if dt != torch.int8 else W.mul(40).clamp(-127, 127).to(torch.int8))
             del W
         for N in w["Ns"]:
-            X = torch.randn(N, K, device=dev, dtype=torch.float32)
+            X = torch.randn(N, M if transposed else K, device=dev, dtype=torch.float32)
             X = X.to(dt) if dt != torch.int8 else X.mul(40).clamp(-127, 127).to(torch.int8)
-            outs = [torch.empty((N, M), dtype=out_dt, device=dev) for _ in Ws]
+            outs = [torch.empty((N, K if transposed else M), dtype=out_dt, device=dev) for _ in Ws]
             try:
                 for W, o in zip(Ws, outs):
                     fn(X, W, o)
@@ -585,20 +609,26 @@ def oracle_sample(w, budget_s: float):
     # rows of the weight in the sample: all of them unless one SpMM pass would blow the budget
     rows = M if M * K * max(w["Ns"]) <= 4e9 else max(128, int(4e9 // (K * max(w["Ns"]))) // 128 * 128)
     sub = A[:rows]
-    Xs = [inputs.raw(inputs.draw(w["ab"], (N, K), 1.0, g)).numpy() for N in w["Ns"]]
+    transposed = w.get("op") == "spmm_t"
+    # the product's right operand for those rows: X [N, K], or dY [N, rows] for the transposed use
+    Xs = [inputs.raw(inputs.draw(w["ab"], (N, rows if transposed else K), 1.0, g)).numpy() for N in w["Ns"]]
     flops, reps = 0.0, 0
     t0 = time.perf_counter()
     while True:
         _, _, ov, om = oracle.prune_compress(w["ab"], sub)
         for N, X in zip(w["Ns"], Xs):
-            oracle.spmm(w["ab"], w["c"], ov, om, X, K)
+            if transposed:
+                oracle.spmm_t(w["ab"], w["c"], ov, om, X, K)
+            else:
+                oracle.spmm(w["ab"], w["c"], ov, om, X, K)
             flops += 2.0 * rows * K * N
         reps += 1
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
+    what = "transposed product dY * W" if transposed else "SpMM"
     return flops, dt, oracle.default_threads(), (
-        f"{reps} x (prune+compress of {rows}x{K} weight rows and SpMM for N in {w['Ns']})")
+        f"{reps} x (prune+compress of {rows}x{K} weight rows and {what} for N in {w['Ns']})")
 
 
 # ---------------------------------------------------------------- one workload's record
@@ -644,7 +674,7 @@ def measure(name, args, rank, world, target_s, cpu_budget_s):
     value = job_tflops(world, flops, pass_ms)
     hbm, bf16_peak, bf16_sus, peak_kind = peaks()
     long_region = args.steps * ms_step >= 1000.0
-    tpeak, tpeak_src = tensor_peak(w["ab"], bf16_peak, bf16_sus, long_region)
+    tpeak, tpeak_src = tensor_peak(w["ab"], bf16_peak, bf16_sus, long_region, dense_op=w.get("op") == "spmm_t")
     hbm_src = f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback"
 
     # Every (shape, N) product group: its bound is the one its arithmetic

@@ -297,6 +297,31 @@ ST24_API st24_status st24_spmm_noalloc(st24_dtype ab_type, st24_dtype c_type, in
                                        const float* row_scale, void* stream);
 
 /*
+ * The transposed use of a compressed weight ([CH26] "2:4: ~2x on the Matmul,
+ * Less End-to-End": after pruning to 2:4 the model is retrained, and the
+ * input gradient of a layer Y = X * A^T is dX = dY * A, a sum over M, along
+ * which A has no 2:4 structure):
+ *
+ *   C(k, n) = alpha * sum_m A(m, k) * B(m, n) + beta * C(k, n)
+ *
+ *   ab_type  : ST24_F16 or ST24_BF16 (fp32 accumulation); c_type: ST24_F32,
+ *              ST24_BF16 or ST24_F16.
+ *   A_values, A_meta : device, the compressed form of A (M x K), as for
+ *              st24_spmm; it is read compressed and expanded on chip.
+ *   B        : device, element (m, n) at B[n*ldb + m] (a row-major dY[N, M],
+ *              ldb >= M).
+ *   C        : device, element (k, n) at C[n*ldc + k] (a row-major dX[N, K],
+ *              ldc >= K); read when beta != 0, always written.
+ * The output is rounded to nearest-even from fp32.  Requirements: K % 128 ==
+ * 0 (ST24_ERR_UNSUPPORTED otherwise); A_values, A_meta and B 16-byte aligned,
+ * ldb*2 % 16 == 0, C aligned to its element size (ST24_ERR_MISALIGNED).  No
+ * workspace.  N or K == 0 is a no-op; M == 0 gives C = beta * C.
+ */
+ST24_API st24_status st24_spmm_t(st24_dtype ab_type, st24_dtype c_type, int64_t M, int64_t N, int64_t K,
+                                 float alpha, const void* A_values, const void* A_meta, const void* B,
+                                 int64_t ldb, float beta, void* C, int64_t ldc, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the status word the kernels
  * of the current device write when a bounded wait runs out
  * (ST24_ERR_TIMEOUT), or returns ST24_ERR_CUDA if the stream reports an

@@ -21,7 +21,7 @@ from . import _build_lib
 __all__ = [
     "St24Error", "load", "st24_version", "st24_status_string", "st24_values_bytes",
     "st24_meta_bytes", "st24_prune_compress", "st24_decompress", "st24_spmm_workspace_bytes",
-    "st24_spmm", "st24_spmm_ex", "st24_spmm_noalloc", "st24_device_status", "dtype_code", "compress", "spmm", "Workspace",
+    "st24_spmm", "st24_spmm_ex", "st24_spmm_noalloc", "st24_spmm_t", "st24_device_status", "dtype_code", "compress", "spmm", "Workspace",
 ]
 
 F16, BF16, E4M3, S8, F32, S32 = 0, 1, 2, 3, 4, 5
@@ -77,6 +77,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.st24_spmm_ex.restype = i
     lib.st24_spmm_noalloc.argtypes = [i, i, i64, i64, i64, f, p, p, p, i64, f, p, i64, p, p]
     lib.st24_spmm_noalloc.restype = i
+    lib.st24_spmm_t.argtypes = [i, i, i64, i64, i64, f, p, p, p, i64, f, p, i64, p]
+    lib.st24_spmm_t.restype = i
     lib.st24_selftest_wait_timeout.argtypes = [p]
     lib.st24_selftest_wait_timeout.restype = i
     lib.st24_device_status.argtypes = [p]
@@ -201,6 +203,19 @@ def st24_spmm(values: torch.Tensor, meta: torch.Tensor, X: torch.Tensor, Y: torc
         _check(load().st24_spmm(*args), "st24_spmm")
     else:
         _check(load().st24_spmm_ex(k, flags, *args), "st24_spmm_ex")
+
+
+def st24_spmm_t(values: torch.Tensor, meta: torch.Tensor, dY: torch.Tensor, dX: torch.Tensor, *, K: int | None = None,
+                alpha: float = 1.0, beta: float = 0.0, M: int | None = None, stream=None) -> None:
+    """dX[N, K] = alpha * dY[N, M] @ A + beta * dX, A (M x K) given by (values, meta)."""
+    N, Mx = dY.shape
+    M = Mx if M is None else M
+    K = dX.shape[1] if K is None else K
+    if dY.stride(1) != 1 or dX.stride(1) != 1:
+        raise ValueError("dY and dX must have unit stride along their last dimension")
+    _check(load().st24_spmm_t(dtype_code(dY.dtype), dtype_code(dX.dtype), M, N, K, float(alpha), _ptr(values),
+                              _ptr(meta), _ptr(dY), dY.stride(0), float(beta), _ptr(dX), dX.stride(0),
+                              _stream(stream)), "st24_spmm_t")
 
 
 def st24_spmm_noalloc(values: torch.Tensor, meta: torch.Tensor, X: torch.Tensor, Y: torch.Tensor, *,

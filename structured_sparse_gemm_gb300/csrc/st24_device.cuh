@@ -353,6 +353,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// D[tmem] (+)= A(smem) * B(smem), dense, 16-bit inputs (the descriptors and
+// the instruction descriptor say which operand is K- or MN-major).
+__device__ __forceinline__ void tc_mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A(smem, 2:4 sparse, metadata in tmem) * B(smem).
 __device__ __forceinline__ void tc_mma_sp_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t meta,
                                               uint32_t idesc, uint32_t accumulate) {
