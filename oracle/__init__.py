@@ -28,6 +28,9 @@ What each function follows (web pages, cited by title and section):
 * ``prune_compress_nm``: the same chapter, section "Block Sparsity, N:M
   Generalizations, and Channel Pruning" (keep N of every M; 1:4, 2:8, ...),
   written in the 2:4 form (reading R8).
+* ``prune_compress_nm2``: the same section, for patterns that keep up to four
+  of a 4-element subgroup (4:8, 3:8), written as two 2:4 forms whose sum is
+  the pruned matrix (reading R10).
 * ``spmm_t`` / ``spmm_t_sampled``: the transposed use of a compressed weight,
   dX = dY * W (the same chapter, section "2:4: ~2x on the Matmul, Less
   End-to-End": retraining after the prune needs the layer's input gradient),
@@ -86,6 +89,7 @@ def lib():
         _lib.orc_spmm_t_sampled.argtypes = [i, i, i64, i64, i64, d, p, p, p, i64, d, p, i64, p, p, i64, p, p, i]
         _lib.orc_quantize_prune_compress.argtypes = [i, i, p, i64, i64, i64, p, p, p, p]
         _lib.orc_prune_compress_nm.argtypes = [i, i, i, p, i64, i64, i64, p, p, p]
+        _lib.orc_prune_compress_nm2.argtypes = [i, i, i, p, i64, i64, i64, p, p, p]
         _lib.orc_enc_e4m3.argtypes = [ctypes.c_float]
         _lib.orc_enc_e4m3.restype = ctypes.c_uint8
         _lib.orc_meta_row_bytes.argtypes = [i64]
@@ -190,6 +194,24 @@ def prune_compress_nm(dt, n: int, m: int, W: np.ndarray):
     rc = lib().orc_prune_compress_nm(dt, n, m, _ptr(W), M, K, K, _ptr(pruned), _ptr(values), _ptr(meta))
     if rc != 0:
         raise ValueError("oracle prune_compress_nm: (n, m) in {1, 2} x {4, 8}, K % m == 0, a known type")
+    return pruned, values, meta
+
+
+def prune_compress_nm2(dt, n: int, m: int, W: np.ndarray):
+    """Keep the n largest |w| of every m along K (n <= 4; reading R10) and write the result
+    as two 2:4 forms concatenated along K.
+
+    Returns (pruned M x K, values M x K -- form 0's K/2 then form 1's K/2 per row,
+    meta M x 2*ceil(K/8) uint8 -- form 0's bytes then form 1's per row)."""
+    dt = _code(dt)
+    W = _as_storage(dt, W)
+    M, K = W.shape
+    pruned = np.empty_like(W)
+    values = np.empty((M, K), W.dtype)
+    meta = np.empty((M, 2 * meta_row_bytes(K)), np.uint8)
+    rc = lib().orc_prune_compress_nm2(dt, n, m, _ptr(W), M, K, K, _ptr(pruned), _ptr(values), _ptr(meta))
+    if rc != 0:
+        raise ValueError("oracle prune_compress_nm2: m in {4, 8}, 1 <= n <= min(4, m), K % m == 0, a known type")
     return pruned, values, meta
 
 

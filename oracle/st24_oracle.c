@@ -45,6 +45,8 @@
  *  R7 the per-row quantisation before the prune (see orc_quantize_prune_compress).
  *  R8 N:M pruning written in the 2:4 form (see orc_prune_compress_nm).
  *  R9 the transposed product sums m in ascending order (see orc_spmm_t).
+ *  R10 N:M pruning with up to four kept per 4-subgroup written as two 2:4
+ *     forms whose sum is the pruned matrix (see orc_prune_compress_nm2).
  */
 #include <math.h>
 #include <pthread.h>
@@ -357,6 +359,85 @@ int orc_prune_compress_nm(int dt, int n, int m, const void* W, int64_t M, int64_
                 }
                 (void)nk;
                 if (meta) meta[r * mrb + g / 2] |= (uint8_t)((i0 | (i1 << 2)) << (4 * (g % 2)));
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * N:M pruning with up to four kept elements per aligned 4-element subgroup
+ * (4:8, 3:8, ...; "Chapter 26 -- Sparsity: The Hardware View", section "Block
+ * Sparsity, N:M Generalizations, and Channel Pruning").  Reading R10: keep the
+ * n largest |w| of every m consecutive elements along K exactly as
+ * orc_prune_compress_nm does (chosen one at a time, ties to the lower index),
+ * then write the result as TWO 2:4 compressed forms whose sum is the pruned
+ * matrix: in every 4-element subgroup the kept elements in ascending index
+ * order go first to form 0 (its first two) and then to form 1 (the rest); a
+ * form holding fewer than two of the subgroup's elements takes as the missing
+ * slots the lowest indices of the subgroup not among its own, with +0 values.
+ * The forms are stored concatenated along K, so that together they are the
+ * 2:4 form of an M x 2K matrix [form 0 | form 1]:
+ *   values (M x K): row r = form 0's K/2 values, then form 1's K/2 values;
+ *   meta   (M x 2*ceil(K/8) bytes): row r = form 0's ceil(K/8) bytes, then form 1's.
+ * Multiplying that M x 2K matrix by B stacked twice ([B; B], 2K x N) gives the
+ * pruned matrix times B.  pruned (M x K, may be NULL) receives W with every
+ * dropped element +0.  Supported: m in {4, 8}, 1 <= n <= min(4, m), K % m == 0.
+ * Returns 0, or -1 for unsupported arguments.
+ */
+int orc_prune_compress_nm2(int dt, int n, int m, const void* W, int64_t M, int64_t K, int64_t ldw,
+                           void* pruned, void* values, uint8_t* meta)
+{
+    int es = elem_size(dt);
+    if (es == 0 || dt == ORC_S32 || dt == ORC_F32 || (m != 4 && m != 8) || n < 1 || n > 4 || n > m || K % m != 0)
+        return -1;
+    const uint8_t* w = (const uint8_t*)W;
+    int64_t mrb = orc_meta_row_bytes(K);
+    if (meta) memset(meta, 0, (size_t)(M * 2 * mrb));
+    for (int64_t r = 0; r < M; ++r) {
+        for (int64_t g0 = 0; g0 < K; g0 += m) {
+            double v[8];
+            int keep[8] = {0};
+            for (int j = 0; j < m; ++j) v[j] = load_real(dt, w + (r * ldw) * es, g0 + j);
+            for (int t = 0; t < n; ++t) {           /* the t-th largest: first maximum not yet kept */
+                int best = -1;
+                for (int j = 0; j < m; ++j)
+                    if (!keep[j] && (best < 0 || mag_greater(v[j], v[best]))) best = j;
+                keep[best] = 1;
+            }
+            for (int j = 0; j < m; ++j) {
+                if (!pruned) continue;
+                uint8_t* dst = (uint8_t*)pruned + (r * K + g0 + j) * es;
+                if (keep[j]) memcpy(dst, w + (r * ldw + g0 + j) * es, es);
+                else memset(dst, 0, es);
+            }
+            for (int q = 0; q < m / 4; ++q) {
+                int kept[4], nk = 0;
+                for (int j = 0; j < 4; ++j)
+                    if (keep[4 * q + j]) kept[nk++] = j;
+                int64_t g = (g0 + 4 * q) / 4;
+                for (int f = 0; f < 2; ++f) {
+                    int own[2], no = 0;                 /* this form's kept elements of the subgroup */
+                    for (int t = 2 * f; t < nk && t < 2 * f + 2; ++t) own[no++] = kept[t];
+                    int idx[2], isval[2], c = 0;
+                    for (int t = 0; t < no; ++t) { idx[c] = own[t]; isval[c] = 1; ++c; }
+                    for (int j = 0; j < 4 && c < 2; ++j) {   /* lowest indices not among its own */
+                        int mine = 0;
+                        for (int t = 0; t < no; ++t) mine |= (own[t] == j);
+                        if (!mine && (c == 0 || idx[0] != j)) { idx[c] = j; isval[c] = 0; ++c; }
+                    }
+                    int lo = idx[0] < idx[1] ? 0 : 1;   /* the pair in ascending index order */
+                    int i0 = idx[lo], i1 = idx[1 - lo];
+                    int v0 = isval[lo], v1 = isval[1 - lo];
+                    if (values) {
+                        uint8_t* vrow = (uint8_t*)values + (r * K + (int64_t)f * (K / 2)) * es;
+                        if (v0) memcpy(vrow + (2 * g) * es, w + (r * ldw + 4 * g + i0) * es, es);
+                        else memset(vrow + (2 * g) * es, 0, es);
+                        if (v1) memcpy(vrow + (2 * g + 1) * es, w + (r * ldw + 4 * g + i1) * es, es);
+                        else memset(vrow + (2 * g + 1) * es, 0, es);
+                    }
+                    if (meta) meta[r * 2 * mrb + f * mrb + g / 2] |= (uint8_t)((i0 | (i1 << 2)) << (4 * (g % 2)));
+                }
             }
         }
     }

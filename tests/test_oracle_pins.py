@@ -481,3 +481,73 @@ def test_transposed_epilogue_and_sampling():
     samp, _ = oracle.spmm_t_sampled("bf16", "bf16", values, meta, dY, K, ks, ns, alpha=0.5, beta=-2.0,
                                     C_in=bits(cin))
     assert np.array_equal(samp, out[ns, ks])
+
+
+# ---- N:M with up to four kept per subgroup, as two 2:4 forms (reading R10) --------
+
+@pytest.mark.parametrize("n", [3, 4])
+@pytest.mark.parametrize("dt", ["bf16", "s8"])
+def test_nm2_bruteforce(dt, n):
+    # tie-heavy rows: the kept set of every 8-group maximises sum |x|, the
+    # lexicographically smallest index set among the maximisers
+    m = 8
+    rng = np.random.default_rng(n)
+    vals = rng.choice([-3, -2, -1, 0, 1, 2, 3], size=(64, 64))
+    W = torch.tensor(vals, dtype=inputs.TORCH_DTYPE[dt])
+    pruned, values, meta = oracle.prune_compress_nm2(dt, n, m, inputs.raw(W).numpy())
+    kept = oracle.decode(dt, pruned).reshape(pruned.shape) != 0
+    mags = np.abs(vals)
+    for r in range(vals.shape[0]):
+        for g0 in range(0, vals.shape[1], m):
+            grp = mags[r, g0:g0 + m]
+            best = max(itertools.combinations(range(m), n), key=lambda c: (sum(grp[list(c)]), [-i for i in c]))
+            want = np.zeros(m, bool)
+            want[list(best)] = True
+            assert np.array_equal(kept[r, g0:g0 + m], want & (grp != 0))
+
+
+@pytest.mark.parametrize("n,m", [(4, 8), (3, 8), (2, 8), (1, 4), (4, 4)])
+@pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3", "s8"])
+def test_nm2_two_forms_sum_to_the_pruned_matrix(dt, n, m):
+    K = 16 * m
+    W = inputs.draw(dt, (29, K), 1.0, inputs.generator(n * m))
+    raw = inputs.raw(W).numpy()
+    pruned, values, meta = oracle.prune_compress_nm2(dt, n, m, raw)
+    mrb = oracle.meta_row_bytes(K)
+    # each half is a valid 2:4 form (ascending index pairs), and the two add up to the pruned matrix
+    f0 = oracle.decompress(dt, np.ascontiguousarray(values[:, :K // 2]), np.ascontiguousarray(meta[:, :mrb]), K)
+    f1 = oracle.decompress(dt, np.ascontiguousarray(values[:, K // 2:]), np.ascontiguousarray(meta[:, mrb:]), K)
+    total = oracle.decode(dt, f0) + oracle.decode(dt, f1)
+    assert np.array_equal(total, oracle.decode(dt, pruned))
+    # no position holds a non-zero in both forms
+    assert not np.any((oracle.decode(dt, f0) != 0) & (oracle.decode(dt, f1) != 0))
+    # exactly n non-zeros per m-group on inputs without zeros among the kept
+    nz = (oracle.decode(dt, pruned) != 0).reshape(29, -1, m).sum(axis=2)
+    assert np.all(nz <= n) and np.mean(nz == n) > 0.95
+    # with n <= 2, form 0 is the one-form result and form 1 is all zeros
+    if n <= 2 and m in (4, 8):
+        p1, v1, m1 = oracle.prune_compress_nm(dt, n, m, raw)
+        assert np.array_equal(values[:, :K // 2].view(np.uint8), v1.view(np.uint8))
+        assert np.array_equal(meta[:, :mrb], m1)
+        assert not np.any(oracle.decode(dt, f1))
+
+
+def test_nm2_product_over_the_stacked_forms():
+    """The two forms as one M x 2K 2:4 matrix times B stacked twice equal the pruned
+    matrix times B (integer-valued inputs: every sum exact in fp64)."""
+    K, M, N = 64, 24, 5
+    g = inputs.generator(8)
+    A = torch.randint(-9, 10, (M, K), generator=g).to(torch.float32).to(torch.bfloat16)
+    X = torch.randint(-9, 10, (N, K), generator=g).to(torch.float32).to(torch.bfloat16)
+    pruned, values, meta = oracle.prune_compress_nm2("bf16", 4, 8, bits(A))
+    X2 = np.concatenate([bits(X), bits(X)], axis=1)          # [N, 2K]: B stacked twice along K
+    sp, _ = oracle.spmm("bf16", "f32", values, meta, X2, 2 * K)
+    de, _ = oracle.gemm_dense("bf16", "f32", pruned, bits(X))
+    assert np.array_equal(sp, de)
+
+
+def test_nm2_rejects_unsupported():
+    W = np.zeros((4, 64), np.uint16)
+    for n, m in [(5, 8), (0, 8), (2, 16), (3, 2)]:
+        with pytest.raises(ValueError):
+            oracle.prune_compress_nm2("bf16", n, m, W)
