@@ -104,7 +104,17 @@ typedef enum st24_spmm_flags {
        while the preceding kernel on the stream is still running, which hides
        the launch-to-launch gap of back-to-back decode-shaped products.  B and C
        are always read only after the preceding kernel has completed. */
-    ST24_SPMM_FIXED_A = 1
+    ST24_SPMM_FIXED_A = 1,
+    /* A_values and A_meta hold TWO 2:4 compressed forms of M x K side by side
+       along K, as written by st24_prune_compress_nm2 (values M x K, meta
+       M x 2*ceil(K/8)): the compressed form of the M x 2K matrix
+       [form 0 | form 1].  The product multiplies it by B read once per form --
+       B's k-coordinate wraps at K -- into one accumulator, so the result is
+       (form 0 + form 1) * B, e.g. a 4:8-pruned weight times B.  K is B's K and
+       must be a multiple of 256 (else ST24_ERR_UNSUPPORTED); the workspace is
+       st24_spmm_workspace_bytes(ab_type, c_type, M, N, 2K) bytes.  Not taken by
+       ST24_KERNEL_MMA_SP_DIRECT. */
+    ST24_SPMM_TWO_FORMS = 2
 } st24_spmm_flags;
 
 /* Library version, (major << 16) | (minor << 8) | patch. */
@@ -160,6 +170,30 @@ ST24_API st24_status st24_prune_compress(st24_dtype type, const void* W, int64_t
  */
 ST24_API st24_status st24_prune_compress_nm(st24_dtype type, int n, int m, const void* W, int64_t M, int64_t K,
                                             int64_t ldw, void* values, void* meta, void* stream);
+
+/*
+ * N:M prune and compress into TWO 2:4 forms, for patterns that keep up to
+ * four of an aligned 4-element subgroup ([CH26] "Block Sparsity, N:M
+ * Generalizations, and Channel Pruning": 4:8, 3:8, ...).  The n largest
+ * magnitudes of every m consecutive weights along K are kept (as for
+ * st24_prune_compress_nm); in each 4-element subgroup the kept elements in
+ * ascending index order go first to form 0 (its first two) and then to form 1
+ * (the rest), a form holding fewer than two of them storing +0 partners at the
+ * lowest indices of the subgroup not among its own.  The two forms are the
+ * pruned matrix's two halves: their sum is the pruned matrix.
+ *   values : device, st24_values_bytes(type, M, 2K) bytes: an M x K row-major
+ *            matrix whose row r is form 0's K/2 values, then form 1's.
+ *   meta   : device, st24_meta_bytes(M, 2K) bytes: row r is form 0's
+ *            ceil(K/8) bytes, then form 1's.
+ * Together they are the compressed form of the M x 2K matrix [form 0 | form 1]:
+ * st24_spmm_ex with ST24_SPMM_TWO_FORMS multiplies it by B (read once per
+ * form) into one accumulator, giving the pruned matrix times B.  Supported:
+ * m in {4, 8}, 1 <= n <= min(4, m) (else ST24_ERR_UNSUPPORTED); K a multiple
+ * of 4 and of m; W aligned to the element size and values to twice it (else
+ * ST24_ERR_MISALIGNED).  M or K == 0 is a no-op.  Bit-exact and deterministic.
+ */
+ST24_API st24_status st24_prune_compress_nm2(st24_dtype type, int n, int m, const void* W, int64_t M, int64_t K,
+                                             int64_t ldw, void* values, void* meta, void* stream);
 
 /*
  * Quantise, then prune and compress ([CH26] "Sparsity + Quantization

@@ -21,12 +21,13 @@ from . import _build_lib
 __all__ = [
     "St24Error", "load", "st24_version", "st24_status_string", "st24_values_bytes",
     "st24_meta_bytes", "st24_prune_compress", "st24_decompress", "st24_spmm_workspace_bytes",
-    "st24_spmm", "st24_spmm_ex", "st24_spmm_noalloc", "st24_spmm_t", "st24_device_status", "dtype_code", "compress", "spmm", "Workspace",
+    "st24_spmm", "st24_spmm_ex", "st24_spmm_noalloc", "st24_spmm_t", "st24_prune_compress_nm2", "compress_nm2", "st24_device_status", "dtype_code", "compress", "spmm", "Workspace",
 ]
 
 F16, BF16, E4M3, S8, F32, S32 = 0, 1, 2, 3, 4, 5
 KERNEL_AUTO, KERNEL_TCGEN05, KERNEL_MMA_SP, KERNEL_MMA_SP_DIRECT, KERNEL_TCGEN05_NARROW = 0, 1, 2, 3, 4
 SPMM_FIXED_A = 1   # st24_spmm_flags: A is fixed weights no in-flight work on the stream writes
+SPMM_TWO_FORMS = 2   # st24_spmm_flags: A is two 2:4 forms side by side (st24_prune_compress_nm2)
 _KERNELS = {"auto": KERNEL_AUTO, "tcgen05": KERNEL_TCGEN05, "mma_sp": KERNEL_MMA_SP,
             "mma_sp_direct": KERNEL_MMA_SP_DIRECT, "tcgen05_narrow": KERNEL_TCGEN05_NARROW}
 _TORCH_CODE = {
@@ -65,6 +66,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.st24_prune_compress.restype = i
     lib.st24_prune_compress_nm.argtypes = [i, i, i, p, i64, i64, i64, p, p, p]
     lib.st24_prune_compress_nm.restype = i
+    lib.st24_prune_compress_nm2.argtypes = [i, i, i, p, i64, i64, i64, p, p, p]
+    lib.st24_prune_compress_nm2.restype = i
     lib.st24_quantize_prune_compress.argtypes = [i, i, p, i64, i64, i64, p, p, p, p]
     lib.st24_quantize_prune_compress.restype = i
     lib.st24_decompress.argtypes = [i, p, p, i64, i64, p, i64, p]
@@ -152,6 +155,17 @@ def st24_prune_compress_nm(W: torch.Tensor, values: torch.Tensor, meta: torch.Te
                                          _ptr(meta), _stream(stream)), "st24_prune_compress_nm")
 
 
+def st24_prune_compress_nm2(W: torch.Tensor, values: torch.Tensor, meta: torch.Tensor, n: int, m: int, *,
+                            stream=None) -> None:
+    """Keep the n largest |w| of every m along K (n <= 4) as two 2:4 forms: values [M, K]
+    (form 0's K/2 then form 1's per row), meta [M, 2 * ceil(K/8)]."""
+    M, K = W.shape
+    if W.stride(1) != 1:
+        raise ValueError("W must have unit stride along K")
+    _check(load().st24_prune_compress_nm2(dtype_code(W.dtype), n, m, _ptr(W), M, K, W.stride(0), _ptr(values),
+                                          _ptr(meta), _stream(stream)), "st24_prune_compress_nm2")
+
+
 def st24_quantize_prune_compress(W: torch.Tensor, values: torch.Tensor, meta: torch.Tensor, scales: torch.Tensor,
                                  *, stream=None) -> None:
     """Quantise each row of W [M, K] (f16/bf16) to values' 8-bit type (e4m3 or int8) with a
@@ -180,14 +194,15 @@ def st24_spmm_workspace_bytes(ab, c, M: int, N: int, K: int) -> int:
 def st24_spmm(values: torch.Tensor, meta: torch.Tensor, X: torch.Tensor, Y: torch.Tensor, *, K: int | None = None,
               alpha: float = 1.0, beta: float = 0.0, row_scale: torch.Tensor | None = None,
               workspace: torch.Tensor | None = None, M: int | None = None, stream=None,
-              kernel: str | int = "auto", fixed_a: bool = False) -> None:
+              kernel: str | int = "auto", fixed_a: bool = False, two_forms: bool = False) -> None:
     """Y[N, M] = alpha * row_scale * (A_sparse @ X.T).T + beta * Y, A given by (values, meta).
 
     ``kernel`` picks the kernel family ("auto", "tcgen05", "mma_sp",
     "mma_sp_direct" or "tcgen05_narrow");
     ``fixed_a`` declares (values, meta) fixed weights that no work still in
-    flight on the stream writes (ST24_SPMM_FIXED_A).  Anything but the
-    defaults goes through st24_spmm_ex."""
+    flight on the stream writes (ST24_SPMM_FIXED_A); ``two_forms`` says they
+    hold two 2:4 forms side by side (ST24_SPMM_TWO_FORMS; K is B's K).
+    Anything but the defaults goes through st24_spmm_ex."""
     N, Kx = X.shape
     K = Kx if K is None else K
     M = Y.shape[1] if M is None else M
@@ -198,7 +213,7 @@ def st24_spmm(values: torch.Tensor, meta: torch.Tensor, X: torch.Tensor, Y: torc
             X.stride(0), float(beta), _ptr(Y), Y.stride(0), _ptr(row_scale), _ptr(workspace), ws_bytes,
             _stream(stream))
     k = _KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
-    flags = SPMM_FIXED_A if fixed_a else 0
+    flags = (SPMM_FIXED_A if fixed_a else 0) | (SPMM_TWO_FORMS if two_forms else 0)
     if k == KERNEL_AUTO and flags == 0:
         _check(load().st24_spmm(*args), "st24_spmm")
     else:
@@ -259,6 +274,15 @@ def compress_nm(W: torch.Tensor, n: int, m: int, *, stream=None):
     values = torch.empty((M, K // 2), dtype=W.dtype, device=W.device)
     meta = torch.empty((M, (K // 4 + 1) // 2), dtype=torch.uint8, device=W.device)
     st24_prune_compress_nm(W, values, meta, n, m, stream=stream)
+    return values, meta
+
+
+def compress_nm2(W: torch.Tensor, n: int, m: int, *, stream=None):
+    """(values [M, K], meta [M, 2 * ceil(K/8)]): the two 2:4 forms of W's n:m pruning."""
+    M, K = W.shape
+    values = torch.empty((M, K), dtype=W.dtype, device=W.device)
+    meta = torch.empty((M, 2 * ((K // 4 + 1) // 2)), dtype=torch.uint8, device=W.device)
+    st24_prune_compress_nm2(W, values, meta, n, m, stream=stream)
     return values, meta
 
 

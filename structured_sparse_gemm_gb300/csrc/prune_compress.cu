@@ -12,6 +12,9 @@
 // values and 32 or 64 contiguous bytes of metadata; four pieces per lane are
 // loaded before any is used, which keeps enough bytes in flight per SM.
 #include "st24_device.cuh"
+#include "st24_schedule.cuh"
+
+#include <type_traits>
 
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -421,41 +424,70 @@ __global__ void __launch_bounds__(kThreads) decompress_any(
 
 bool aligned(const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// ---- N:M prune into the 2:4 form -----------------------------------------
+// ---- N:M prune into one or two 2:4 forms -----------------------------------
 // ("Chapter 26 -- Sparsity: The Hardware View", section "Block Sparsity, N:M
 // Generalizations, and Channel Pruning": keep N of every M consecutive
-// weights.)  In every group of m elements along K the n of largest
-// magnitude are kept (the order of mag_key; ties to the lower index).  With
-// m = 4 or 8 and n <= 2 each aligned 4-element subgroup keeps at most two,
-// so the result is a 2:4 compressed form (+0 partners at the lowest dropped
-// indices) that st24_spmm multiplies exactly.  One thread per 8 elements of
-// a row (two subgroups: one metadata byte); neighbouring threads take
-// neighbouring elements, so the warp's loads and stores are contiguous.
-template <int DT, int ES>
+// weights.)  In every group of M_ elements along K the N_ of largest
+// magnitude are kept (the order of mag_key; ties to the lower index).  Each
+// aligned 4-element subgroup then holds some of the kept elements in
+// ascending index order: the first two go to form 0, the rest (TWO: up to two
+// more, for N_ up to 4) to form 1; a form holding fewer than two of a
+// subgroup's elements takes as the missing slots the lowest indices of the
+// subgroup not among its own, with +0 values.  With N_ <= 2 form 0 is the
+// whole result, a 2:4 compressed form st24_spmm multiplies exactly; with two
+// forms (values M x K and metadata M x 2 ceil(K/8), form 0 then form 1 in
+// each row) the forms together are the 2:4 form of an M x 2K matrix whose
+// product with B stacked twice is the pruned matrix times B.  One thread per
+// 8 elements of a row (two subgroups: one metadata byte per form);
+// neighbouring threads take neighbouring elements, so the warp's loads and
+// stores are contiguous.
+
+// The pair a form stores for one subgroup: its own kept elements (bits of
+// `own`, at most two) and the lowest other indices as +0 fillers, ascending.
+__device__ __forceinline__ void form_pair(uint32_t own, int& i0, int& i1, bool& v0, bool& v1) {
+  int idx[2] = {0, 0};
+  bool isv[2] = {false, false};
+  int c = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (((own >> j) & 1u) && c < 2) { idx[c] = j; isv[c] = true; ++c; }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (c < 2 && !((own >> j) & 1u) && (c == 0 || idx[0] != j)) { idx[c] = j; isv[c] = false; ++c; }
+  const bool lo = idx[0] < idx[1];
+  i0 = lo ? idx[0] : idx[1];
+  i1 = lo ? idx[1] : idx[0];
+  v0 = lo ? isv[0] : isv[1];
+  v1 = lo ? isv[1] : isv[0];
+}
+
+template <int DT, int ES, int N_, int M_, bool TWO>
 __global__ void __launch_bounds__(kThreads) prune_compress_nm_kernel(const uint8_t* __restrict__ W, int64_t w_row_bytes,
-                                                                     int64_t M, int64_t K, int n, int m,
-                                                                     uint8_t* __restrict__ values,
+                                                                     int64_t M, int64_t K, uint8_t* __restrict__ values,
                                                                      uint8_t* __restrict__ meta, int vec) {
+  static_assert(M_ == 4 || M_ == 8, "group size");
+  static_assert(N_ >= 1 && N_ <= (TWO ? 4 : 2) && N_ <= M_, "kept per group");
   const int64_t upr = (K + 7) / 8;   // 8-element units per row
   const int64_t total = M * upr;
   const int64_t mrb = meta_row_bytes(K);
+  const int64_t vrow = TWO ? K : K / 2;          // values per row (both forms)
+  const int64_t erow = TWO ? 2 * mrb : mrb;      // metadata bytes per row (both forms)
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < total;
        u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = u / upr, c0 = (u - r * upr) * 8;
+    const int64_t r = div_nn(u, upr), c0 = (u - r * upr) * 8;
     const int cnt = K - c0 < 8 ? static_cast<int>(K - c0) : 8;   // 4 or 8
     const uint8_t* src = W + r * w_row_bytes + c0 * ES;
     uint32_t e[8], k[8];
     if (vec && cnt == 8) {
       // the unit in one load (16-byte aligned rows of 16-bit values, 8-byte of 8-bit ones)
-      uint32_t w[4];
       if constexpr (ES == 2) {
         const uint4 v = __ldcs(reinterpret_cast<const uint4*>(src));
-        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) e[j] = (w[j / 2] >> (16 * (j & 1))) & 0xFFFFu;
       } else {
         const uint2 v = __ldcs(reinterpret_cast<const uint2*>(src));
-        w[0] = v.x; w[1] = v.y;
+        const uint32_t w[2] = {v.x, v.y};
 #pragma unroll
         for (int j = 0; j < 8; ++j) e[j] = (w[j / 4] >> (8 * (j & 3))) & 0xFFu;
       }
@@ -468,39 +500,49 @@ __global__ void __launch_bounds__(kThreads) prune_compress_nm_kernel(const uint8
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) k[j] = mag_key<DT>(e[j]);
-    bool keep[8];
+    uint32_t kept = 0;   // bit j: element j of the unit is kept
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
+      constexpr int m = M_;
       const int b = (j / m) * m;   // this element's m-group inside the unit
       int above = 0;               // elements of the group that outrank it
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         if (i >= b && i < b + m && i != j && (k[i] > k[j] || (k[i] == k[j] && i < j))) ++above;
-      keep[j] = j < cnt && above < n;
+      if (j < cnt && above < N_) kept |= 1u << j;
     }
-    uint32_t mb = 0;
-    uint8_t* vrow = values + r * (K / 2) * ES;
+    uint32_t mb[2] = {0u, 0u};
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       if (4 * q >= cnt) break;
-      int idx[2] = {0, 0}, c = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (keep[4 * q + j] && c < 2) idx[c++] = j;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (!keep[4 * q + j] && c < 2 && (c == 0 || j != idx[0])) idx[c++] = j;
-      const int i0 = idx[0] < idx[1] ? idx[0] : idx[1], i1 = idx[0] < idx[1] ? idx[1] : idx[0];
-      const uint32_t v0 = keep[4 * q + i0] ? e[4 * q + i0] : 0u, v1 = keep[4 * q + i1] ? e[4 * q + i1] : 0u;
-      const int64_t col = c0 / 2 + 2 * q;   // value column of the pair
-      if constexpr (ES == 2) {
-        *reinterpret_cast<uint32_t*>(vrow + col * 2) = v0 | (v1 << 16);
+      const uint32_t km = (kept >> (4 * q)) & 0xFu;
+      uint32_t own[2];
+      if constexpr (TWO) {
+        const uint32_t b1 = km & (0u - km), rest = km ^ b1, b2 = rest & (0u - rest);
+        own[0] = b1 | b2;        // the subgroup's first two kept elements
+        own[1] = km & ~own[0];   // the rest
       } else {
-        *reinterpret_cast<uint16_t*>(vrow + col) = static_cast<uint16_t>(v0 | (v1 << 8));
+        own[0] = km;
+        own[1] = 0u;
       }
-      mb |= static_cast<uint32_t>(i0 | (i1 << 2)) << (4 * q);
+#pragma unroll
+      for (int f = 0; f < (TWO ? 2 : 1); ++f) {
+        int i0, i1;
+        bool v0, v1;
+        form_pair(own[f], i0, i1, v0, v1);
+        const uint32_t a0 = v0 ? e[4 * q + i0] : 0u, a1 = v1 ? e[4 * q + i1] : 0u;
+        uint8_t* vrow_ptr = values + (r * vrow + f * (K / 2)) * ES;
+        const int64_t col = c0 / 2 + 2 * q;   // value column of the pair
+        if constexpr (ES == 2) {
+          *reinterpret_cast<uint32_t*>(vrow_ptr + col * 2) = a0 | (a1 << 16);
+        } else {
+          *reinterpret_cast<uint16_t*>(vrow_ptr + col) = static_cast<uint16_t>(a0 | (a1 << 8));
+        }
+        mb[f] |= static_cast<uint32_t>(i0 | (i1 << 2)) << (4 * q);
+      }
     }
-    meta[r * mrb + c0 / 8] = static_cast<uint8_t>(mb);
+    meta[r * erow + c0 / 8] = static_cast<uint8_t>(mb[0]);
+    if constexpr (TWO) meta[r * erow + mrb + c0 / 8] = static_cast<uint8_t>(mb[1]);
   }
 }
 
@@ -724,8 +766,8 @@ st24_status launch_prune_compress(int dt, const void* W, int64_t M, int64_t K, i
   return cudaGetLastError() == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;
 }
 
-st24_status launch_prune_compress_nm(int dt, int n, int m, const void* W, int64_t M, int64_t K, int64_t ldw,
-                                     void* values, void* meta, cudaStream_t stream) {
+st24_status launch_prune_compress_nm(int dt, int n, int m, bool two, const void* W, int64_t M, int64_t K,
+                                     int64_t ldw, void* values, void* meta, cudaStream_t stream) {
   const DeviceInfo* dev = current_device_info();
   if (!dev) return ST24_ERR_CUDA;
   const int64_t units = M * ((K + 7) / 8);
@@ -733,16 +775,30 @@ st24_status launch_prune_compress_nm(int dt, int n, int m, const void* W, int64_
     const int va = 8 * es;   // bytes of one unit: its vector load needs this alignment
     const int vec = aligned(W, va) && (ldw * es) % va == 0 ? 1 : 0;
     kern<<<grid_for(kern, units, kThreads, dev->num_sms), kThreads, 0, stream>>>(
-        static_cast<const uint8_t*>(W), ldw * es, M, K, n, m, static_cast<uint8_t*>(values),
-        static_cast<uint8_t*>(meta), vec);
+        static_cast<const uint8_t*>(W), ldw * es, M, K, static_cast<uint8_t*>(values), static_cast<uint8_t*>(meta),
+        vec);
+    return true;
   };
+  // (n, m, two) -> the compiled pattern, for one element type
+  auto pattern = [&](auto dtc, auto esc) {
+    constexpr int DT = decltype(dtc)::value, ES = decltype(esc)::value;
+#define ST24_NM(N_, M_, TWO)                                                                  \
+  if (n == N_ && m == M_ && two == TWO) return go(prune_compress_nm_kernel<DT, ES, N_, M_, TWO>, ES);
+    ST24_NM(1, 4, false) ST24_NM(2, 4, false) ST24_NM(1, 8, false) ST24_NM(2, 8, false)
+    ST24_NM(1, 4, true) ST24_NM(2, 4, true) ST24_NM(3, 4, true) ST24_NM(4, 4, true)
+    ST24_NM(1, 8, true) ST24_NM(2, 8, true) ST24_NM(3, 8, true) ST24_NM(4, 8, true)
+#undef ST24_NM
+    return false;
+  };
+  bool ok = false;
   switch (dt) {
-    case kF16: go(prune_compress_nm_kernel<kF16, 2>, 2); break;
-    case kBF16: go(prune_compress_nm_kernel<kBF16, 2>, 2); break;
-    case kE4M3: go(prune_compress_nm_kernel<kE4M3, 1>, 1); break;
-    case kS8: go(prune_compress_nm_kernel<kS8, 1>, 1); break;
-    default: return ST24_ERR_UNSUPPORTED;
+    case kF16: ok = pattern(std::integral_constant<int, kF16>{}, std::integral_constant<int, 2>{}); break;
+    case kBF16: ok = pattern(std::integral_constant<int, kBF16>{}, std::integral_constant<int, 2>{}); break;
+    case kE4M3: ok = pattern(std::integral_constant<int, kE4M3>{}, std::integral_constant<int, 1>{}); break;
+    case kS8: ok = pattern(std::integral_constant<int, kS8>{}, std::integral_constant<int, 1>{}); break;
+    default: break;
   }
+  if (!ok) return ST24_ERR_UNSUPPORTED;
   return cudaGetLastError() == cudaSuccess ? ST24_OK : ST24_ERR_CUDA;
 }
 

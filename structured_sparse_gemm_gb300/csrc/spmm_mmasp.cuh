@@ -95,6 +95,7 @@ struct Params : OutParams {
   int b_evict_first;      // B likewise (the raster keeps the A panel resident instead)
   int a_fixed;            // A is not written by earlier work on the stream: load it before the dependency wait
   int b3d;                // tmB is 3-D (128-byte K chunk, row, chunk index): one copy per stage
+  int64_t kb_wrap;        // two-form product: k-blocks per form (B's k-block of k-block kb is kb mod kb_wrap); 0: one form
   int cluster;            // > 1: the CTAs of each split tile form a cluster and reduce in shared memory
   float* partials;       // [2 * gridDim.x][PARTIAL_ELEMS]
   unsigned* counters;    // one per output tile
@@ -246,7 +247,6 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
         for (int64_t kb = kb0; kb < kb1; ++kb, ++done) {
           const uint32_t fb = smem_u32(&full_bar[stage]);
           uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
-          const int32_t kB = static_cast<int32_t>(kb * T::BK);           // logical K
           if (done >= preloaded) {
             if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) { ok = false; break; }
             mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
@@ -257,10 +257,12 @@ __global__ void __launch_bounds__((Config<DT, BN, WARPS_N, STAGES, WMT>::THREADS
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
+          const int64_t kbb = (p.kb_wrap && kb >= p.kb_wrap) ? kb - p.kb_wrap : kb;
           if (p.b3d) {
             // Both 128-byte-wide K chunks of the stage in one copy (3-D map).
-            tma_load_3d(smem_u32(st + Cfg::A_BYTES), &tmB, 0, nt * BN, static_cast<int32_t>(2 * kb), fb, reuse);
+            tma_load_3d(smem_u32(st + Cfg::A_BYTES), &tmB, 0, nt * BN, static_cast<int32_t>(2 * kbb), fb, reuse);
           } else {
+            const int32_t kB = static_cast<int32_t>(kbb * T::BK);
             tma_load_2d(smem_u32(st + Cfg::A_BYTES), &tmB, kB, nt * BN, fb, reuse);
             tma_load_2d(smem_u32(st + Cfg::A_BYTES + BN * 128), &tmB, kB + 128 / T::ES, nt * BN, fb, reuse);
           }
@@ -590,7 +592,7 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
                             CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tensor_map_2d(&tmE, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.meta, a.K / 8, a.M, a.K / 8,
                             T::EB, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !encode_tensor_map_2d(&tmB, ty, a.B, a.K, a.N, a.ldb * T::ES, 128 / T::ES, BN,
+      !encode_tensor_map_2d(&tmB, ty, a.B, a.Kb ? a.Kb : a.K, a.N, a.ldb * T::ES, 128 / T::ES, BN,
                             CU_TENSOR_MAP_SWIZZLE_128B))
     return ST24_ERR_CUDA;
   // B as (128-byte K chunk, row, chunk index): a stage's two chunks in one
@@ -599,7 +601,7 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
   // decode-shaped products.
   CUtensorMap tmB3;
   const uint64_t bdims[3] = {static_cast<uint64_t>(128 / T::ES), static_cast<uint64_t>(a.N),
-                             static_cast<uint64_t>(a.K / (128 / T::ES))};
+                             static_cast<uint64_t>((a.Kb ? a.Kb : a.K) / (128 / T::ES))};
   const uint64_t bstrides[2] = {static_cast<uint64_t>(a.ldb * T::ES), 128};
   const uint32_t bbox[3] = {128u / T::ES, static_cast<uint32_t>(BN), 2u};
   const bool b3d = encode_tensor_map_3d(&tmB3, ty, a.B, bdims, bstrides, bbox, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -607,6 +609,7 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
   Params p{};
   p.b3d = b3d ? 1 : 0;
   p.M = a.M; p.N = a.N; p.K = a.K;
+  p.kb_wrap = (a.Kb && a.Kb != a.K) ? a.Kb / T::BK : 0;
   p.tiles_m = plan.tiles_m;
   p.tiles_n = plan.tiles_n;
   p.group_m = plan.group_m;

@@ -96,6 +96,7 @@ struct Params : OutParams {
   int64_t k_iters;   // k-blocks (stages) of the whole K
   int parts;         // S: CTAs per tile = cluster size (1, 2, 4 or 8)
   int a_fixed;       // load weight stages before the dependency wait
+  int64_t kb_wrap;   // two-form product: k-blocks per form (B's k-block of k-block kb is kb mod kb_wrap); 0: one form
   unsigned* status;
 };
 
@@ -199,9 +200,10 @@ __global__ void __launch_bounds__(320, 2)
         issued |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
         const uint32_t bb = smem_u32(&fullb_bar[stage]);
+        const int64_t kbb = (p.kb_wrap && kb >= p.kb_wrap) ? kb - p.kb_wrap : kb;
         mbar_arrive_expect_tx(bb, Cfg::B_BYTES);
         tma_load_3d(smem_u32(smem + stage * Cfg::STAGE_BYTES + Cfg::A_BYTES), &tmB, 0, 0,
-                    static_cast<int32_t>(kb * 2 * C), bb, reuse);
+                    static_cast<int32_t>(kbb * 2 * C), bb, reuse);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
       // Never leave with copies in flight into this CTA's shared memory.

@@ -21,7 +21,7 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
                             static_cast<uint32_t>(C)};
   // B likewise: (128-byte chunk of a column of B, column n, chunk index), 2C chunks per stage.
   const uint64_t bdims[3] = {static_cast<uint64_t>(T::CHUNK_ELEMS), static_cast<uint64_t>(a.N),
-                             static_cast<uint64_t>(a.K) * T::ES / 128};
+                             static_cast<uint64_t>(a.Kb ? a.Kb : a.K) * T::ES / 128};
   const uint64_t bstr[2] = {static_cast<uint64_t>(a.ldb) * T::ES, 128};
   const uint32_t bbox[3] = {static_cast<uint32_t>(T::CHUNK_ELEMS), static_cast<uint32_t>(BN),
                             static_cast<uint32_t>(2 * C)};
@@ -38,6 +38,7 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
   p.row_scale = a.row_scale;
   p.k_iters = plan.k_iters;
   p.parts = plan.cluster;
+  p.kb_wrap = (a.Kb && a.Kb != a.K) ? a.Kb / plan.bk : 0;
   p.a_fixed = (a.flags & ST24_SPMM_FIXED_A) ? 1 : 0;
   p.status = dev.status;
   auto kern = spmm_nt_kernel<DT, BN, C, STAGES, SPLIT>;

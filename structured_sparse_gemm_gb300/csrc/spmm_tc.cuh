@@ -90,6 +90,7 @@ struct TcParams : OutParams {
   int a_evict_first;      // A is streamed once (by the tiles running at the same time): evict it first
   int b_evict_first;      // B likewise (the raster keeps the A panel resident instead)
   int a_fixed;            // A is not written by earlier work on the stream: load it before the dependency wait
+  int64_t kb_wrap;        // two-form product: k-blocks per form (B's k-block of k-block kb is kb mod kb_wrap); 0: one form
   float* partials;
   unsigned* counters;
   unsigned* status;
@@ -222,7 +223,8 @@ __global__ void __launch_bounds__(320, 1)
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
-          const int32_t kB = static_cast<int32_t>(kb * T::BK);
+          const int64_t kbb = (p.kb_wrap && kb >= p.kb_wrap) ? kb - p.kb_wrap : kb;
+          const int32_t kB = static_cast<int32_t>(kbb * T::BK);
           tma_load_2d(smem_u32(st + Cfg::A_BYTES), &tmB, kB, nt * BN, fb, reuse);
           tma_load_2d(smem_u32(st + Cfg::A_BYTES + BN * 128), &tmB, kB + 128 / T::ES, nt * BN, fb, reuse);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -416,7 +418,8 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
                             CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tensor_map_2d(&tmE, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.meta, a.K / 8, a.M, a.K / 8, 16, Cfg::BM,
                             CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !encode_tensor_map_2d(&tmB, ty, a.B, a.K, a.N, a.ldb * T::ES, 128 / T::ES, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+      !encode_tensor_map_2d(&tmB, ty, a.B, a.Kb ? a.Kb : a.K, a.N, a.ldb * T::ES, 128 / T::ES, BN,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
     return ST24_ERR_CUDA;
   // C (element (m, n) at C[n*ldc + m]) as an M-inner 2-D tensor, for the L2
   // prefetch of each tile's C block when beta != 0.
@@ -433,6 +436,7 @@ st24_status launch_cfg(const SpmmArgs& a, const StreamKPlan& plan, const DeviceI
   TcParams p{};
   p.prefetch_c = have_c ? 1 : 0;
   p.M = a.M; p.N = a.N; p.K = a.K;
+  p.kb_wrap = (a.Kb && a.Kb != a.K) ? a.Kb / T::BK : 0;
   p.alpha = a.alpha; p.beta = a.beta;
   p.C = a.C; p.ldc = a.ldc; p.c_type = a.c;
   p.row_scale = a.row_scale;

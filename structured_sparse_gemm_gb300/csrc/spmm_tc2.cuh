@@ -190,7 +190,8 @@ __global__ void __launch_bounds__(320, 1)
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
-          const int32_t kB = static_cast<int32_t>(kb * T::BK);
+          const int64_t kbb = (p.kb_wrap && kb >= p.kb_wrap) ? kb - p.kb_wrap : kb;
+          const int32_t kB = static_cast<int32_t>(kbb * T::BK);
           tma_load_2d(smem_u32(st + Cfg::A_BYTES), &tmB, kB, n0, fb, reuse);
           tma_load_2d(smem_u32(st + Cfg::A_BYTES + Cfg::BH * 128), &tmB, kB + 128 / T::ES, n0, fb, reuse);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -489,7 +490,7 @@ st24_status launch_pair(const SpmmArgs& a, const StreamKPlan& plan, const Device
                             CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tensor_map_2d(&tmE, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.meta, a.K / 8, a.M, a.K / 8, 16, Cfg::BM,
                             CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !encode_tensor_map_2d(&tmB, ty, a.B, a.K, a.N, a.ldb * T::ES, 128 / T::ES, Cfg::BH,
+      !encode_tensor_map_2d(&tmB, ty, a.B, a.Kb ? a.Kb : a.K, a.N, a.ldb * T::ES, 128 / T::ES, Cfg::BH,
                             CU_TENSOR_MAP_SWIZZLE_128B))
     return ST24_ERR_CUDA;
   // C (element (m, n) at C[n*ldc + m]) as an M-inner 2-D tensor: 32 x 32
@@ -509,6 +510,7 @@ st24_status launch_pair(const SpmmArgs& a, const StreamKPlan& plan, const Device
   p.c_tma = c_map ? 1 : 0;
   p.prefetch_c = c_prefetch ? 1 : 0;
   p.M = a.M; p.N = a.N; p.K = a.K;
+  p.kb_wrap = (a.Kb && a.Kb != a.K) ? a.Kb / T::BK : 0;
   p.alpha = a.alpha; p.beta = a.beta;
   p.C = a.C; p.ldc = a.ldc; p.c_type = a.c;
   p.row_scale = a.row_scale;

@@ -256,7 +256,19 @@ st24_status st24_prune_compress_nm(st24_dtype type, int n, int m, const void* W,
   if (!W || !values || !meta || ldw < K) return ST24_ERR_INVALID_ARG;
   const int es = elem_size(type);
   if (!aligned(W, es) || !aligned(values, 2 * es)) return ST24_ERR_MISALIGNED;
-  return launch_prune_compress_nm(type, n, m, W, M, K, ldw, values, meta, static_cast<cudaStream_t>(stream));
+  return launch_prune_compress_nm(type, n, m, false, W, M, K, ldw, values, meta, static_cast<cudaStream_t>(stream));
+}
+
+st24_status st24_prune_compress_nm2(st24_dtype type, int n, int m, const void* W, int64_t M, int64_t K, int64_t ldw,
+                                    void* values, void* meta, void* stream) {
+  if (!is_ab_type(type) || M < 0 || K < 0 || K % 4 != 0) return ST24_ERR_INVALID_ARG;
+  if ((m != 4 && m != 8) || n < 1 || n > 4 || n > m) return ST24_ERR_UNSUPPORTED;
+  if (K % m != 0) return ST24_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return ST24_OK;
+  if (!W || !values || !meta || ldw < K) return ST24_ERR_INVALID_ARG;
+  const int es = elem_size(type);
+  if (!aligned(W, es) || !aligned(values, 2 * es)) return ST24_ERR_MISALIGNED;
+  return launch_prune_compress_nm(type, n, m, true, W, M, K, ldw, values, meta, static_cast<cudaStream_t>(stream));
 }
 
 st24_status st24_quantize_prune_compress(st24_dtype src_type, st24_dtype dst_type, const void* W, int64_t M,
@@ -315,7 +327,8 @@ st24_status st24_spmm_ex(st24_kernel kernel, unsigned flags, st24_dtype ab_type,
   if (kernel != ST24_KERNEL_AUTO && kernel != ST24_KERNEL_TCGEN05 && kernel != ST24_KERNEL_MMA_SP &&
       kernel != ST24_KERNEL_MMA_SP_DIRECT && kernel != ST24_KERNEL_TCGEN05_NARROW)
     return ST24_ERR_INVALID_ARG;
-  if (flags & ~static_cast<unsigned>(ST24_SPMM_FIXED_A)) return ST24_ERR_INVALID_ARG;
+  if (flags & ~static_cast<unsigned>(ST24_SPMM_FIXED_A | ST24_SPMM_TWO_FORMS)) return ST24_ERR_INVALID_ARG;
+  const bool two = (flags & ST24_SPMM_TWO_FORMS) != 0;
   SpmmArgs a{};
   a.flags = flags;
   a.ab = ab_type;
@@ -334,16 +347,32 @@ st24_status st24_spmm_ex(st24_kernel kernel, unsigned flags, st24_dtype ab_type,
   a.row_scale = row_scale;
   a.workspace = workspace;
   a.ws_bytes = ws_bytes;
-  st24_status st = check_spmm_args(a);
+  a.Kb = K;
+  st24_status st = check_spmm_args(a);   // B and C as for K
   if (st != ST24_OK || M == 0 || N == 0) return st;
+  if (two) {
+    // A holds two 2:4 forms of M x K side by side: the M x 2K matrix [form 0 | form 1],
+    // multiplied by B once per form (B's k-coordinate wraps at K).
+    if (K % 256 != 0) return ST24_ERR_UNSUPPORTED;
+    if (kernel == ST24_KERNEL_MMA_SP_DIRECT) return ST24_ERR_UNSUPPORTED;
+    a.K = 2 * K;
+  }
   if (kernel == ST24_KERNEL_TCGEN05 && ab_type == ST24_S8) return ST24_ERR_UNSUPPORTED;
   if (kernel == ST24_KERNEL_MMA_SP_DIRECT && !direct_applies(a)) return ST24_ERR_UNSUPPORTED;
   if (kernel == ST24_KERNEL_TCGEN05_NARROW && !narrow_applies(a)) return ST24_ERR_UNSUPPORTED;
   const DeviceInfo* dev = current_device_info();
   if (!dev) return ST24_ERR_CUDA;
-  const int k = resolve_kernel(kernel, a, dev->num_sms);
+  int k = resolve_kernel(kernel, a, dev->num_sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return launch_scale_c(a, *dev, s);
+  if (two) {
+    // every k-block must lie in one form: the plan's k-block must divide K
+    if (k == ST24_KERNEL_MMA_SP_DIRECT) k = ST24_KERNEL_TCGEN05_NARROW;
+    if (plan_for(k, a, dev->num_sms).bk <= 0 || K % plan_for(k, a, dev->num_sms).bk != 0) {
+      if (kernel != ST24_KERNEL_AUTO) return ST24_ERR_UNSUPPORTED;
+      k = ab_type == ST24_S8 || ab_type == ST24_F16 || ab_type == ST24_BF16 ? ST24_KERNEL_MMA_SP : ST24_KERNEL_TCGEN05;
+    }
+  }
   if (k == ST24_KERNEL_MMA_SP_DIRECT) return launch_spmm_direct(a, *dev, s);
   const StreamKPlan plan = plan_for(k, a, dev->num_sms);
   if (plan.ws_bytes > 0 && (!workspace || ws_bytes < plan.ws_bytes || !aligned(workspace, 16)))

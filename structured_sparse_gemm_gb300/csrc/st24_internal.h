@@ -41,8 +41,9 @@ const DeviceInfo* current_device_info();
 // ---------------------------------------------------------- prune / compress
 st24_status launch_prune_compress(int dt, const void* W, int64_t M, int64_t K, int64_t ldw,
                                   void* values, void* meta, cudaStream_t stream);
-st24_status launch_prune_compress_nm(int dt, int n, int m, const void* W, int64_t M, int64_t K, int64_t ldw,
-                                     void* values, void* meta, cudaStream_t stream);
+// N:M prune into one 2:4 form (two = false, n <= 2) or two (two = true, n <= 4).
+st24_status launch_prune_compress_nm(int dt, int n, int m, bool two, const void* W, int64_t M, int64_t K,
+                                     int64_t ldw, void* values, void* meta, cudaStream_t stream);
 st24_status launch_quantize_prune_compress(int src, int dst, const void* W, int64_t M, int64_t K, int64_t ldw,
                                            void* values, void* meta, float* scales, cudaStream_t stream);
 st24_status launch_decompress(int dt, const void* values, const void* meta, int64_t M, int64_t K,
@@ -51,7 +52,8 @@ st24_status launch_decompress(int dt, const void* values, const void* meta, int6
 // ---------------------------------------------------------------- SpMM
 struct SpmmArgs {
   int ab, c;
-  int64_t M, N, K;
+  int64_t M, N, K;         // K: A's extent along K (twice B's for a two-form product)
+  int64_t Kb;              // K of B (the contraction); 0 means K
   float alpha, beta;
   const void* values;
   const void* meta;

@@ -133,6 +133,16 @@ def test_direct_kernel_rejects_what_it_does_not_cover(lib):
         assert call(ab, c, 33) == 2
 
 
+def test_two_forms_flag_checks(lib):
+    # two 2:4 forms side by side: K must be a multiple of 256, and the register-direct family declines them
+    def call(kernel, K):
+        return lib.st24_spmm_ex(kernel, st.SPMM_TWO_FORMS, st.BF16, st.BF16, 128, 8, K, 1.0, FAKE, FAKE, FAKE, K, 0.0,
+                                FAKE, 128, None, None, 0, None)
+
+    assert call(st.KERNEL_AUTO, 384) == 2
+    assert call(st.KERNEL_MMA_SP_DIRECT, 512) == 2
+
+
 def test_narrow_kernel_rejects_what_it_does_not_cover(lib):
     # the narrow tcgen05 family takes 1 <= N <= 64 and no int8 (no int8 tcgen05 kind on sm_103a)
     def call(ab, c, N):
@@ -151,6 +161,6 @@ def test_spmm_ex_rejects_unknown_kernel_and_flags(lib):
 
     assert call(kernel=5) == 1
     assert call(kernel=-1) == 1
-    assert call(flags=2) == 1
+    assert call(flags=4) == 1
     assert call(flags=1 << 31) == 1
     assert call(kernel=7, flags=1) == 1
