@@ -372,7 +372,14 @@ def extra_prune_timings(w, stream, dev):
         nbytes = M * K * 2 + M * K // 2 * 2 + M * K // 8
         out[f"prune_compress_nm_{n}of{m}_bf16"] = {"us_per_launch": us, "GB/s": nbytes / (us * 1e-6) / 1e9,
                                                    "bytes": nbytes}
-    del Wb, vb, mb
+    del vb, mb
+    # 4:8 as two 2:4 forms (values M x K, metadata M x 2 K/8)
+    v2 = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    m2 = torch.empty((M, K // 4), dtype=torch.uint8, device=dev)
+    us = time_launches(lambda: st.st24_prune_compress_nm2(Wb, v2, m2, 4, 8, stream=stream), stream)
+    nbytes = M * K * 2 + M * K * 2 + M * K // 4
+    out["prune_compress_nm2_4of8_bf16"] = {"us_per_launch": us, "GB/s": nbytes / (us * 1e-6) / 1e9, "bytes": nbytes}
+    del Wb, v2, m2
     return out
 
 
