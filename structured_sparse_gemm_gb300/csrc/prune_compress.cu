@@ -269,14 +269,16 @@ __device__ __forceinline__ uint4 expand_piece(const uint2 vals, uint32_t meta_bi
 }
 
 constexpr int kThreads = 256;
-constexpr int kPiecesPerLane = 4;
+constexpr int kPiecesPerLane = 2;
 constexpr int kWarpSpan = 32 * kPiecesPerLane;  // pieces one warp handles per iteration
 
 // Fast path.  The matrix is a sequence of 16-byte pieces, `ppr` per row; warp
-// w handles pieces [w*128, w*128+128) of each grid-stride round, lane l the
-// pieces l, l+32, l+64 and l+96 of that span.  A lane divides once per round
-// (Idx is 32-bit whenever the piece count allows) and carries (row, col)
-// forward for its other pieces.
+// w handles pieces [w*64, w*64+64) of each grid-stride round, lane l the
+// pieces l and l+32 of that span.  Piece p (counted row by row)
+// owns bytes [8p, 8p+8) of the values and its metadata at p * (16 / ES / 8)
+// bytes, since both outputs are dense; only the input may have a row stride.
+// Where it has one, a lane divides once per round (Idx is 32-bit whenever the
+// piece count allows) and carries (row, col) forward for its other pieces.
 template <typename Idx>
 __device__ __forceinline__ void advance(Idx& row, Idx& col, Idx step, Idx ppr) {
   col += step;
@@ -289,71 +291,79 @@ __device__ __forceinline__ void advance(Idx& row, Idx& col, Idx step, Idx ppr) {
 template <int DT, int ES, typename Idx>
 __global__ void __launch_bounds__(kThreads) prune_compress_vec(
     const uint8_t* __restrict__ W, int64_t w_row_bytes, Idx total, Idx ppr,
-    uint8_t* __restrict__ values, int64_t v_row_bytes, uint8_t* __restrict__ meta,
-    int64_t m_row_bytes) {
+    uint8_t* __restrict__ values, uint8_t* __restrict__ meta) {
   const int lane = threadIdx.x & 31;
   const Idx warp = (static_cast<Idx>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const Idx nwarps = (static_cast<Idx>(gridDim.x) * kThreads) >> 5;
+  const bool dense = w_row_bytes == static_cast<int64_t>(ppr) * 16;
   for (Idx base = warp * kWarpSpan; base < total; base += nwarps * kWarpSpan) {
     uint4 in[kPiecesPerLane];
-    Idx row[kPiecesPerLane], col[kPiecesPerLane];
-    Idx r = (base + lane) / ppr, c = base + lane - r * ppr;
+    if (dense) {
 #pragma unroll
-    for (int i = 0; i < kPiecesPerLane; ++i) {
-      row[i] = r;
-      col[i] = c;
-      if (base + i * 32 + lane < total)
-        in[i] = __ldcs(reinterpret_cast<const uint4*>(W + static_cast<int64_t>(r) * w_row_bytes +
-                                                      static_cast<int64_t>(c) * 16));
-      advance<Idx>(r, c, 32, ppr);
+      for (int i = 0; i < kPiecesPerLane; ++i) {
+        const Idx q = base + i * 32 + lane;
+        if (q < total) in[i] = __ldcs(reinterpret_cast<const uint4*>(W) + q);
+      }
+    } else {
+      Idx r = (base + lane) / ppr, c = base + lane - r * ppr;
+#pragma unroll
+      for (int i = 0; i < kPiecesPerLane; ++i) {
+        if (base + i * 32 + lane < total)
+          in[i] = __ldcs(reinterpret_cast<const uint4*>(W + static_cast<int64_t>(r) * w_row_bytes) + c);
+        advance<Idx>(r, c, 32, ppr);
+      }
     }
 #pragma unroll
     for (int i = 0; i < kPiecesPerLane; ++i) {
-      if (base + i * 32 + lane >= total) break;
+      const Idx q = base + i * 32 + lane;
+      if (q >= total) break;
       uint32_t mb;
       uint2 v;
       if (!compress_piece_lanes<DT, ES>(in[i], v, mb)) v = compress_piece<DT, ES>(in[i], mb);
-      const int64_t rr = row[i], cc = col[i];
-      *reinterpret_cast<uint2*>(values + rr * v_row_bytes + cc * 8) = v;
+      reinterpret_cast<uint2*>(values)[q] = v;
       if constexpr (ES == 2)
-        meta[rr * m_row_bytes + cc] = static_cast<uint8_t>(mb);
+        meta[q] = static_cast<uint8_t>(mb);
       else
-        *reinterpret_cast<uint16_t*>(meta + rr * m_row_bytes + cc * 2) = static_cast<uint16_t>(mb);
+        reinterpret_cast<uint16_t*>(meta)[q] = static_cast<uint16_t>(mb);
     }
   }
 }
 
 template <int ES, typename Idx>
 __global__ void __launch_bounds__(kThreads) decompress_vec(
-    const uint8_t* __restrict__ values, int64_t v_row_bytes, const uint8_t* __restrict__ meta,
-    int64_t m_row_bytes, Idx total, Idx ppr, uint8_t* __restrict__ W, int64_t w_row_bytes) {
+    const uint8_t* __restrict__ values, const uint8_t* __restrict__ meta, Idx total, Idx ppr,
+    uint8_t* __restrict__ W, int64_t w_row_bytes) {
   const int lane = threadIdx.x & 31;
   const Idx warp = (static_cast<Idx>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const Idx nwarps = (static_cast<Idx>(gridDim.x) * kThreads) >> 5;
+  const bool dense = w_row_bytes == static_cast<int64_t>(ppr) * 16;
   for (Idx base = warp * kWarpSpan; base < total; base += nwarps * kWarpSpan) {
     uint2 v[kPiecesPerLane];
     uint32_t mb[kPiecesPerLane];
-    Idx row[kPiecesPerLane], col[kPiecesPerLane];
-    Idx r = (base + lane) / ppr, c = base + lane - r * ppr;
 #pragma unroll
     for (int i = 0; i < kPiecesPerLane; ++i) {
-      row[i] = r;
-      col[i] = c;
-      if (base + i * 32 + lane < total) {
-        const int64_t rr = r, cc = c;
-        v[i] = __ldcs(reinterpret_cast<const uint2*>(values + rr * v_row_bytes + cc * 8));
+      const Idx q = base + i * 32 + lane;
+      if (q < total) {
+        v[i] = __ldcs(reinterpret_cast<const uint2*>(values) + q);
         if constexpr (ES == 2)
-          mb[i] = __ldcs(meta + rr * m_row_bytes + cc);
+          mb[i] = __ldcs(meta + q);
         else
-          mb[i] = __ldcs(reinterpret_cast<const uint16_t*>(meta + rr * m_row_bytes + cc * 2));
+          mb[i] = __ldcs(reinterpret_cast<const uint16_t*>(meta) + q);
       }
-      advance<Idx>(r, c, 32, ppr);
+    }
+    Idx r = 0, c = 0;
+    if (!dense) {
+      r = (base + lane) / ppr;
+      c = base + lane - r * ppr;
     }
 #pragma unroll
     for (int i = 0; i < kPiecesPerLane; ++i) {
-      if (base + i * 32 + lane >= total) break;
-      const int64_t rr = row[i], cc = col[i];
-      *reinterpret_cast<uint4*>(W + rr * w_row_bytes + cc * 16) = expand_piece<ES>(v[i], mb[i]);
+      const Idx q = base + i * 32 + lane;
+      if (q >= total) break;
+      uint4* dst = dense ? reinterpret_cast<uint4*>(W) + q
+                         : reinterpret_cast<uint4*>(W + static_cast<int64_t>(r) * w_row_bytes) + c;
+      *dst = expand_piece<ES>(v[i], mb[i]);
+      if (!dense) advance<Idx>(r, c, 32, ppr);
     }
   }
 }
@@ -555,8 +565,9 @@ __global__ void __launch_bounds__(kThreads) prune_compress_nm_kernel(const uint8
 // Quantization Combine": 2:4 sparsity and 8-bit weights stack.)  The codes
 // of each 16-value piece are then pruned and compressed like an 8-bit
 // weight's.  One CTA per row (grid-stride over rows): when the row fits in
-// registers (K <= 256 threads x 4 pieces x 16), it is read once.
-constexpr int kQPieces = 4;   // 16-value pieces per thread held in registers
+// registers (K <= 256 threads x QP pieces x 16, QP = 1, 2 or 4: the fewest
+// that hold it, so short rows keep the register count and occupancy up), it
+// is read once.
 
 template <int ST>
 __device__ __forceinline__ float to_f32(uint32_t bits16) {
@@ -604,7 +615,7 @@ __device__ __forceinline__ uint4 quantize16(const uint4 lo, const uint4 hi, floa
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-template <int ST, int DT, bool FITS>
+template <int ST, int DT, int QP>
 __global__ void __launch_bounds__(kThreads) quantize_prune_compress_rows(
     const uint8_t* __restrict__ W, int64_t w_row_bytes, int64_t M, int64_t K, uint8_t* __restrict__ values,
     uint8_t* __restrict__ meta, float* __restrict__ scales) {
@@ -613,11 +624,12 @@ __global__ void __launch_bounds__(kThreads) quantize_prune_compress_rows(
   const float Q = DT == kE4M3 ? 448.0f : 127.0f;
   for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
     const uint8_t* row = W + m * w_row_bytes;
-    uint4 held[FITS ? kQPieces : 1][2];
+    constexpr bool FITS = QP > 0;
+    uint4 held[FITS ? QP : 1][2];
     float amax = 0.0f;
     if constexpr (FITS) {
 #pragma unroll
-      for (int i = 0; i < kQPieces; ++i) {
+      for (int i = 0; i < QP; ++i) {
         const int64_t pc = threadIdx.x + static_cast<int64_t>(i) * kThreads;
         if (pc < P) {
           held[i][0] = __ldcs(reinterpret_cast<const uint4*>(row + pc * 32));
@@ -625,7 +637,7 @@ __global__ void __launch_bounds__(kThreads) quantize_prune_compress_rows(
         }
       }
 #pragma unroll
-      for (int i = 0; i < kQPieces; ++i)
+      for (int i = 0; i < QP; ++i)
         if (threadIdx.x + static_cast<int64_t>(i) * kThreads < P)
           amax = absmax8<ST>(held[i][1], absmax8<ST>(held[i][0], amax));
     } else {
@@ -656,7 +668,7 @@ __global__ void __launch_bounds__(kThreads) quantize_prune_compress_rows(
     };
     if constexpr (FITS) {
 #pragma unroll
-      for (int i = 0; i < kQPieces; ++i) {
+      for (int i = 0; i < QP; ++i) {
         const int64_t pc = threadIdx.x + static_cast<int64_t>(i) * kThreads;
         if (pc < P) emit(pc, held[i][0], held[i][1]);
       }
@@ -704,12 +716,11 @@ void launch_pc(const void* W, int64_t M, int64_t K, int64_t ldw, void* values, v
     if (fits_u32(total)) {
       auto k = prune_compress_vec<DT, ES, uint32_t>;
       k<<<grid_for(k, total, kThreads / 32 * kWarpSpan, num_sms), kThreads, 0, s>>>(
-          w, ldw * ES, static_cast<uint32_t>(total), static_cast<uint32_t>(ppr), v, (K / 2) * ES, e,
-          meta_row_bytes(K));
+          w, ldw * ES, static_cast<uint32_t>(total), static_cast<uint32_t>(ppr), v, e);
     } else {
       auto k = prune_compress_vec<DT, ES, int64_t>;
       k<<<grid_for(k, total, kThreads / 32 * kWarpSpan, num_sms), kThreads, 0, s>>>(
-          w, ldw * ES, total, ppr, v, (K / 2) * ES, e, meta_row_bytes(K));
+          w, ldw * ES, total, ppr, v, e);
     }
   } else {
     auto k = prune_compress_any<DT, ES>;
@@ -729,12 +740,11 @@ void launch_dc(const void* values, const void* meta, int64_t M, int64_t K, void*
     if (fits_u32(total)) {
       auto k = decompress_vec<ES, uint32_t>;
       k<<<grid_for(k, total, kThreads / 32 * kWarpSpan, num_sms), kThreads, 0, s>>>(
-          v, (K / 2) * ES, e, meta_row_bytes(K), static_cast<uint32_t>(total), static_cast<uint32_t>(ppr), w,
-          ldw * ES);
+          v, e, static_cast<uint32_t>(total), static_cast<uint32_t>(ppr), w, ldw * ES);
     } else {
       auto k = decompress_vec<ES, int64_t>;
       k<<<grid_for(k, total, kThreads / 32 * kWarpSpan, num_sms), kThreads, 0, s>>>(
-          v, (K / 2) * ES, e, meta_row_bytes(K), total, ppr, w, ldw * ES);
+          v, e, total, ppr, w, ldw * ES);
     }
   } else {
     auto k = decompress_any<ES>;
@@ -806,7 +816,8 @@ st24_status launch_quantize_prune_compress(int src, int dst, const void* W, int6
                                            void* values, void* meta, float* scales, cudaStream_t stream) {
   const DeviceInfo* dev = current_device_info();
   if (!dev) return ST24_ERR_CUDA;
-  const bool fits = K <= static_cast<int64_t>(kThreads) * kQPieces * 16;
+  const int64_t per_piece = static_cast<int64_t>(kThreads) * 16;   // K covered by one piece per thread
+  const int qp = K <= per_piece ? 1 : K <= 2 * per_piece ? 2 : K <= 4 * per_piece ? 4 : 0;
   const auto* w = static_cast<const uint8_t*>(W);
   auto* v = static_cast<uint8_t*>(values);
   auto* e = static_cast<uint8_t*>(meta);
@@ -817,8 +828,10 @@ st24_status launch_quantize_prune_compress(int src, int dst, const void* W, int6
   };
 #define ST24_QPC(S, D)                                                          \
   if (src == S && dst == D) {                                                  \
-    if (fits) go(quantize_prune_compress_rows<S, D, true>);                    \
-    else go(quantize_prune_compress_rows<S, D, false>);                        \
+    if (qp == 1) go(quantize_prune_compress_rows<S, D, 1>);                    \
+    else if (qp == 2) go(quantize_prune_compress_rows<S, D, 2>);               \
+    else if (qp == 4) go(quantize_prune_compress_rows<S, D, 4>);               \
+    else go(quantize_prune_compress_rows<S, D, 0>);                            \
   }
   ST24_QPC(kBF16, kE4M3) else ST24_QPC(kBF16, kS8) else ST24_QPC(kF16, kE4M3) else ST24_QPC(kF16, kS8) else
     return ST24_ERR_UNSUPPORTED;
