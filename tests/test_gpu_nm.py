@@ -177,3 +177,75 @@ def test_two_form_fp8_full_size_sampled(N):
     X2 = np.concatenate([bits(X), bits(X)], axis=1)
     ref, _ = oracle.spmm_sampled("e4m3", "bf16", ov, om, X2, 2 * K, rows, cols)
     assert_close(decode_out(Y)[cols, rows], ref, "e4m3", "bf16", f"4:8 fp8 N={N} sampled")
+
+
+# ---- special values and strides on the lanes kernel ---------------------------
+
+def _special_weight(dt, M, K, seed):
+    g = torch.Generator().manual_seed(seed)
+    if dt == "s8":
+        # int8 -128 (|-128| = 128) sends its pieces unit by unit; the rest stay on lanes
+        vals = torch.tensor([-128, -127, -1, 0, 1, 127], dtype=torch.int8)
+        W = vals[torch.randint(0, len(vals), (M, K), generator=g)]
+        W[: M // 2] = torch.where(W[: M // 2] == -128, torch.tensor(-127, dtype=torch.int8), W[: M // 2])
+        return W
+    vals = torch.tensor([0.0, -0.0, 0.5, -0.5, 1.0, -1.0, 2.0, float("nan"), float("inf")])
+    if dt == "e4m3":
+        vals = vals[:8]   # no infinity in e4m3
+    W = vals[torch.randint(0, len(vals), (M, K), generator=g)].to(inputs.TORCH_DTYPE[dt])
+    if dt != "e4m3":
+        W[: M // 2] = torch.where(torch.isnan(W[: M // 2].float()), torch.zeros((), dtype=W.dtype), W[: M // 2])
+        raw = inputs.raw(W)   # NaNs with different payloads tie with each other
+        raw[M - 1, 0:8] = torch.tensor([0x7FC1, 0x7FC3, 0x3C00, 0x7FC2, 0, 0x7FC5, 0x7FC4, 1],
+                                       dtype=torch.int32).to(raw.dtype)
+    return W
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3", "s8"])
+@pytest.mark.parametrize("n,m", [(1, 4), (2, 8), (1, 8)])
+def test_special_values(dt, n, m):
+    W = _special_weight(dt, 96, 512, n + m)
+    values, meta = st.compress_nm(W.to(DEV), n, m)
+    _, ov, om = oracle.prune_compress_nm(dt, n, m, bits(W))
+    assert np.array_equal(bits(values).view(np.uint8), ov.view(np.uint8))
+    assert np.array_equal(meta.cpu().numpy(), om)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "e4m3", "s8"])
+@pytest.mark.parametrize("n,m", [(4, 8), (3, 8), (3, 4)])
+def test_two_forms_special_values(dt, n, m):
+    W = _special_weight(dt, 96, 512, 10 + n + m)
+    values, meta = st.compress_nm2(W.to(DEV), n, m)
+    _, ov, om = oracle.prune_compress_nm2(dt, n, m, bits(W))
+    assert np.array_equal(bits(values).view(np.uint8), ov.view(np.uint8))
+    assert np.array_equal(meta.cpu().numpy(), om)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "e4m3"])
+@pytest.mark.parametrize("two", [False, True])
+def test_padded_row_stride(dt, two):
+    # rows 16-byte aligned but longer than K: the lanes kernel reads row by row
+    M, K, pad = 70, 1024, 64
+    full = inputs.draw(dt, (M, K + pad), 0.02 if dt == "e4m3" else 1.0, inputs.generator(7))
+    Wd = full.to(DEV)[:, :K]
+    assert Wd.stride(0) == K + pad
+    n, m = (4, 8) if two else (2, 8)
+    fn, ref = (st.compress_nm2, oracle.prune_compress_nm2) if two else (st.compress_nm, oracle.prune_compress_nm)
+    values, meta = fn(Wd, n, m)
+    _, ov, om = ref(dt, n, m, bits(full[:, :K].contiguous()))
+    assert np.array_equal(bits(values).view(np.uint8), ov.view(np.uint8))
+    assert np.array_equal(meta.cpu().numpy(), om)
+
+
+@pytest.mark.parametrize("two", [False, True])
+def test_odd_piece_count(two):
+    # a piece count that is not a multiple of the 64 a warp takes per round: the last
+    # lanes hold one piece or none
+    M, K = 3, 40   # 15 pieces of bf16
+    W = inputs.draw("bf16", (M, K), 1.0, inputs.generator(11))
+    n, m = (3, 8) if two else (1, 8)
+    fn, ref = (st.compress_nm2, oracle.prune_compress_nm2) if two else (st.compress_nm, oracle.prune_compress_nm)
+    values, meta = fn(W.to(DEV), n, m)
+    _, ov, om = ref("bf16", n, m, bits(W))
+    assert np.array_equal(bits(values).view(np.uint8), ov.view(np.uint8))
+    assert np.array_equal(meta.cpu().numpy(), om)
