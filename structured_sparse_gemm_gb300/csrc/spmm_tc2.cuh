@@ -10,19 +10,25 @@
 // products: the pipeline's bytes in flight per SM against L2 latency.
 //
 // Roles (320 threads per CTA, both CTAs):
-//  * warp 0, TMA producer: its CTA's 128 rows of compressed A and metadata and
-//    its BNP / 2 rows of B per stage, on its own full/empty barriers.
-//  * warps 6-9, metadata: shared memory -> this CTA's TMEM (as in the one-CTA
-//    kernel), then signal the leader CTA's meta barrier: the leader's warps
-//    arrive on it (4 arrivals, each expecting 4 bytes), the peer's warps
-//    complete those bytes with an asynchronous 4-byte store into the leader's
-//    shared memory (st.async, whose barrier signal releases at cluster scope
-//    without stalling the warp; a blocking remote arrive cost ~1 us per stage).
-//    Each metadata warp signals only after its own CTA's stage has landed.
-//  * warp 1 of the leader (cluster rank 0), MMA issuer: waits on the meta
-//    barrier, issues the pair MMAs and commits them to the empty barriers and
-//    accumulator barriers of both CTAs (multicast).  Warp 1 of each CTA
-//    allocates and frees TMEM (cta_group::2, both CTAs together).
+//  * warp 0, TMA producer: per stage, first its CTA's metadata (on its own
+//    metadata barrier), then its 128 rows of compressed A and its BNP / 2 rows
+//    of B.  The A and B loads of both CTAs complete on the leader's full
+//    barrier (the cta_group::2 form of the tensor load), which the leader's
+//    producer arms for the bytes of both; each CTA refills a stage when its
+//    own empty barrier (the MMA commit, multicast) says it is free.
+//  * warps 6-9, metadata: once this CTA's metadata has landed, shared memory
+//    -> this CTA's TMEM (as in the one-CTA kernel), then signal the leader
+//    CTA's meta barrier: the leader's warps arrive on it (4 arrivals, each
+//    expecting 4 bytes), the peer's warps complete those bytes with an
+//    asynchronous 4-byte store into the leader's shared memory (st.async,
+//    whose barrier signal releases at cluster scope without stalling the
+//    warp).  The metadata is small and loaded first, so this path runs ahead
+//    of the operand bytes instead of after them.
+//  * warp 1 of the leader (cluster rank 0), MMA issuer: waits on the full
+//    barrier (operands of both CTAs) and the meta barrier, issues the pair
+//    MMAs and commits them to the empty barriers and accumulator barriers of
+//    both CTAs (multicast).  Warp 1 of each CTA allocates and frees TMEM
+//    (cta_group::2, both CTAs together).
 //  * warps 2-5, epilogue: this CTA's 128 rows of the accumulator; they arrive
 //    on the leader's accumulator-empty barrier (8 arrivals).  With beta != 0
 //    each warp stages its 32 x 32 chunks of C in shared memory by TMA, one
@@ -50,6 +56,7 @@ struct PairConfig {
   static constexpr int B_BYTES = BH * 256;           // two 128-byte-wide boxes of BH rows
   static constexpr int E_BYTES = BM * T::EB;
   static constexpr int STAGE_TX = A_BYTES + B_BYTES + E_BYTES;
+  static constexpr int PAIR_TX = 2 * (A_BYTES + B_BYTES);   // operand bytes of both CTAs per stage
   static constexpr int STAGE_BYTES = (STAGE_TX + 1023) / 1024 * 1024;
   static constexpr int META_COL0 = 2 * BNP;          // after the two accumulators
   static constexpr int TMEM_COLS = 512;
@@ -63,7 +70,7 @@ struct PairConfig {
   static_assert(BNP % 32 == 0 && BNP >= 64 && BNP <= 256, "N of the pair MMA; B halves of whole swizzle atoms");
   static_assert(2 * BNP + STAGES * T::META_COLS <= TMEM_COLS, "tensor memory");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-  static_assert((3 * STAGES + 5 + 8) * 8 + 8 + STAGES * 16 <= 512, "barrier region");
+  static_assert((4 * STAGES + 5 + 8) * 8 + 8 + STAGES * 16 <= 512, "barrier region");
 };
 
 template <int DT, int BNP, int STAGES>
@@ -78,9 +85,10 @@ __global__ void __launch_bounds__(320, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* cbuf = smem + STAGES * Cfg::STAGE_BYTES;   // [4 warps][2][CBUF_BYTES] staged chunks of C
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(cbuf + Cfg::C_BYTES);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(cbuf + Cfg::C_BYTES);   // [STAGES] leader: A and B of both CTAs
   uint64_t* empty_bar = full_bar + STAGES;
-  uint64_t* meta_bar = empty_bar + STAGES;      // [STAGES] leader: metadata of both CTAs in TMEM
+  uint64_t* efull_bar = empty_bar + STAGES;     // [STAGES] this CTA's metadata landed
+  uint64_t* meta_bar = efull_bar + STAGES;      // [STAGES] leader: metadata of both CTAs in TMEM
   uint64_t* tfull_bar = meta_bar + STAGES;      // [2] accumulator ready
   uint64_t* tempty_bar = tfull_bar + 2;         // [2] leader: accumulator drained in both CTAs
   uint64_t* drain_bar = tempty_bar + 2;
@@ -98,6 +106,7 @@ __global__ void __launch_bounds__(320, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
+      mbar_init(smem_u32(&efull_bar[s]), 1);
       mbar_init(smem_u32(&meta_bar[s]), 4);
     }
     for (int b = 0; b < 2; ++b) {
@@ -134,12 +143,18 @@ __global__ void __launch_bounds__(320, 1)
       const uint64_t stream_once = p.a_evict_first ? policy_evict_first() : policy_evict_last();
       const uint64_t reuse = p.b_evict_first ? policy_evict_first() : policy_evict_last();
       uint32_t issued = 0, issued_parity = 0;   // per stage (bit s): a copy was issued, and its phase
-      auto load_weights = [&](uint8_t* st, uint32_t fb, int64_t kb, int32_t m0) {
-        tma_load_2d(smem_u32(st), &tmA, static_cast<int32_t>(kb * (128 / T::ES)), m0, fb, stream_once);
+      // Arm stage s (the leader: for both CTAs' operand bytes) and load its
+      // metadata, then its A rows; B follows after the dependency wait.
+      auto load_weights = [&](int s, int64_t kb, int32_t m0) {
+        uint8_t* st = smem + s * Cfg::STAGE_BYTES;
+        const uint32_t fb = smem_u32(&full_bar[s]), eb = smem_u32(&efull_bar[s]);
+        if (rank == 0) mbar_arrive_expect_tx(fb, Cfg::PAIR_TX);
+        mbar_arrive_expect_tx(eb, Cfg::E_BYTES);
         uint8_t* se = st + Cfg::A_BYTES + Cfg::B_BYTES;
         const int32_t ke = static_cast<int32_t>(kb * T::EB);
-        tma_load_2d(smem_u32(se), &tmE, ke, m0, fb, stream_once);
-        if constexpr (T::EB == 32) tma_load_2d(smem_u32(se + 2048), &tmE, ke + 16, m0, fb, stream_once);
+        tma_load_2d(smem_u32(se), &tmE, ke, m0, eb, stream_once);
+        if constexpr (T::EB == 32) tma_load_2d(smem_u32(se + 2048), &tmE, ke + 16, m0, eb, stream_once);
+        tma_load_2d_pair(smem_u32(st), &tmA, static_cast<int32_t>(kb * (128 / T::ES)), m0, fb, 0, stream_once);
       };
       int preloaded = 0;
       {
@@ -152,9 +167,7 @@ __global__ void __launch_bounds__(320, 1)
           const int32_t m0 = static_cast<int32_t>((2 * mt + rank) * Cfg::BM);
           for (int64_t kb = sg.kb0; kb < sg.kb1 && warm > 0; ++kb) {
             if (p.a_fixed && preloaded < STAGES) {
-              const uint32_t fb = smem_u32(&full_bar[preloaded]);
-              mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
-              load_weights(smem + preloaded * Cfg::STAGE_BYTES, fb, kb, m0);
+              load_weights(preloaded, kb, m0);
               issued |= 1u << preloaded;
               ++preloaded;
             } else {
@@ -185,66 +198,90 @@ __global__ void __launch_bounds__(320, 1)
           uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
           if (done >= preloaded) {
             if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) { ok = false; break; }
-            mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
-            load_weights(st, fb, kb, m0);
+            load_weights(stage, kb, m0);
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
           const int64_t kbb = (p.kb_wrap && kb >= p.kb_wrap) ? kb - p.kb_wrap : kb;
           const int32_t kB = static_cast<int32_t>(kbb * T::BK);
-          tma_load_2d(smem_u32(st + Cfg::A_BYTES), &tmB, kB, n0, fb, reuse);
-          tma_load_2d(smem_u32(st + Cfg::A_BYTES + Cfg::BH * 128), &tmB, kB + 128 / T::ES, n0, fb, reuse);
+          tma_load_2d_pair(smem_u32(st + Cfg::A_BYTES), &tmB, kB, n0, fb, 0, reuse);
+          tma_load_2d_pair(smem_u32(st + Cfg::A_BYTES + Cfg::BH * 128), &tmB, kB + 128 / T::ES, n0, fb, 0, reuse);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         have = sch.next(sg);
         if (have) tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt64, nt64);
       }
+      // No copy may still be landing when the CTA exits: the leader's full
+      // barrier counts both CTAs' operand bytes (the peer waits for the
+      // leader at the final cluster barrier), each CTA's metadata barrier its own.
       for (int s = 0; s < STAGES; ++s)
-        if ((issued >> s) & 1u) mbar_wait(smem_u32(&full_bar[s]), (issued_parity >> s) & 1u, p.status);
+        if ((issued >> s) & 1u) {
+          const uint32_t par = (issued_parity >> s) & 1u;
+          if (rank == 0) mbar_wait_cluster(smem_u32(&full_bar[s]), par, p.status);
+          mbar_wait(smem_u32(&efull_bar[s]), par, p.status);
+        }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader)
-    if (lane == 0 && rank == 0) {
+    // The whole warp runs the loop, so the addresses and descriptors are
+    // warp-uniform; one elected lane issues the MMAs and commits (issued from
+    // a single-lane branch, every operand had to be moved to the uniform
+    // datapath per instruction, which made the issue, not the tensor pipe,
+    // the limit).
+    if (rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int abuf = 0;
       uint32_t aphase = 0;
       bool ok = true;
+      const uint32_t smem0 = smem_u32(smem);
+      // whole K-steps in the last k-block (every other k-block has 4)
+      const int64_t k_last = p.K - (KI - 1) * T::BK;
+      const int ksteps_last = k_last / T::KSTEP < 4 ? static_cast<int>(k_last / T::KSTEP) : 4;
       Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, pair);
       Segment sg;
       while (ok && sch.next(sg)) {
-        if (!mbar_wait_cluster(smem_u32(&tempty_bar[abuf]), aphase ^ 1u, p.status)) { ok = false; break; }
+        ok = __all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(&tempty_bar[abuf]), aphase ^ 1u, p.status));
+        if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(abuf * BNP);
         for (int64_t kb = sg.kb0; kb < sg.kb1; ++kb) {
-          // Both CTAs' metadata warps arrive only after their own stage landed.
-          if (!mbar_wait_cluster(smem_u32(&meta_bar[stage]), phase, p.status)) { ok = false; break; }
+          // The operands of both CTAs, then the metadata of both in TMEM.
+          ok = __all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(&full_bar[stage]), phase, p.status) &&
+                                           mbar_wait_cluster(smem_u32(&meta_bar[stage]), phase, p.status));
+          if (!ok) break;
           tc_fence_after();
-          uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
+          const uint32_t a0 = smem0 + static_cast<uint32_t>(stage * Cfg::STAGE_BYTES);
+          const uint64_t da = smem_desc(a0, 16, 1024, kSwizzle128B);
+          const uint64_t db = smem_desc(a0 + Cfg::A_BYTES, 16, 1024, kSwizzle128B);
           const uint32_t mcol = tmem + static_cast<uint32_t>(Cfg::META_COL0 + stage * T::META_COLS);
-          const int64_t ks_left = (p.K - kb * T::BK) / T::KSTEP;
-          const int ksteps = ks_left < 4 ? static_cast<int>(ks_left) : 4;
-          const uint32_t a0 = smem_u32(st), b0 = smem_u32(st + Cfg::A_BYTES);
+          const int ksteps = kb == KI - 1 ? ksteps_last : 4;
+          if (elect_one_lane()) {
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            if (ks >= ksteps) break;
-            const uint64_t da = smem_desc(a0 + ks * 32, 16, 1024, kSwizzle128B);
-            const uint64_t db = smem_desc(b0 + (ks >> 1) * (Cfg::BH * 128) + (ks & 1) * 64, 16, 1024, kSwizzle128B);
-            const uint32_t acc = (kb > sg.kb0 || ks > 0) ? 1u : 0u;
-            if constexpr (T::ES == 2)
-              tc_mma_sp_f16_pair(d, da, db, mcol + 4 * ks, Cfg::IDESC, acc);
-            else
-              tc_mma_sp_f8f6f4_pair(d, da, db, mcol + 4 * ks, Cfg::IDESC, acc);
+            for (int ks = 0; ks < 4; ++ks) {
+              if (ks >= ksteps) break;
+              // descriptor start addresses advance in 16-byte units (no carry: shared memory < 256 KB)
+              const uint64_t dak = da + static_cast<uint64_t>(ks * 2);
+              const uint64_t dbk = db + static_cast<uint64_t>(((ks >> 1) * (Cfg::BH * 128) + (ks & 1) * 64) >> 4);
+              const uint32_t acc = (kb > sg.kb0 || ks > 0) ? 1u : 0u;
+              if constexpr (T::ES == 2)
+                tc_mma_sp_f16_pair(d, dak, dbk, mcol + 4 * ks, Cfg::IDESC, acc);
+              else
+                tc_mma_sp_f8f6f4_pair(d, dak, dbk, mcol + 4 * ks, Cfg::IDESC, acc);
+            }
+            tc_commit_pair(smem_u32(&empty_bar[stage]), kBoth);
           }
-          tc_commit_pair(smem_u32(&empty_bar[stage]), kBoth);
+          __syncwarp();
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit_pair(smem_u32(&tfull_bar[abuf]), kBoth);
+        if (elect_one_lane()) tc_commit_pair(smem_u32(&tfull_bar[abuf]), kBoth);
+        __syncwarp();
         if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
       }
       // Both CTAs learn when every pair MMA has completed (before TMEM is freed).
-      tc_commit_pair(smem_u32(drain_bar), kBoth);
+      if (elect_one_lane()) tc_commit_pair(smem_u32(drain_bar), kBoth);
+      __syncwarp();
       mbar_wait(smem_u32(drain_bar), 0, p.status);
     } else if (lane == 0) {
       mbar_wait(smem_u32(drain_bar), 0, p.status);
@@ -264,7 +301,7 @@ __global__ void __launch_bounds__(320, 1)
       tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
       const int64_t rows_valid = p.M - (2 * mt + rank) * Cfg::BM;   // rows past M hold zero-filled metadata
       for (int64_t kb = sg.kb0; kb < sg.kb1; ++kb) {
-        if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.status)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(&efull_bar[stage]), phase, p.status)) { ok = false; break; }
         const uint8_t* se = smem + stage * Cfg::STAGE_BYTES + Cfg::A_BYTES + Cfg::B_BYTES;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) +
                                static_cast<uint32_t>(Cfg::META_COL0 + stage * T::META_COLS);

@@ -165,6 +165,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// The same load issued by either CTA of a CTA pair (cta_group::2), its bytes
+// completing on the barrier at the offset of `bar` in CTA `rank` of the
+// cluster: both CTAs' operand loads can signal the one barrier that the
+// pair's MMA issuer waits on.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t x, int32_t y,
+                                                 uint32_t bar, uint32_t rank, uint64_t policy) {
+  uint32_t rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(bar), "r"(rank));
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(rb), "l"(policy)
+      : "memory");
+}
+
 // Prefetch the box at (x, y) of a tensor map into L2 (no shared memory, no
 // completion to wait for).  A prefetch only warms L2, the point of coherence,
 // so it is safe even for data another kernel may still be writing.
@@ -315,6 +330,15 @@ __device__ __forceinline__ void tc_mma_sp_f8f6f4_pair(uint32_t d, uint64_t a, ui
       "l"(a), "l"(b), "r"(meta), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// True in exactly one lane of a converged warp (the lowest).  Warp-wide code
+// keeps its values warp-uniform, and the elected lane issues the tcgen05
+// instruction that needs only one thread.
+__device__ __forceinline__ bool elect_one_lane() {
+  uint32_t elected;
+  asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(elected));
+  return elected != 0;
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
