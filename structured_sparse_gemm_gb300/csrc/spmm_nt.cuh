@@ -215,39 +215,49 @@ __global__ void __launch_bounds__(320, 2)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int64_t kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait(smem_u32(&meta_bar[stage]), phase, p.status) ||
-            !mbar_wait(smem_u32(&fulla_bar[stage]), phase, p.status) ||
-            !mbar_wait(smem_u32(&fullb_bar[stage]), phase, p.status))
-          break;
-        tc_fence_after();
-        const uint32_t a0 = smem_u32(smem + stage * Cfg::STAGE_BYTES);
-        const uint32_t b0 = a0 + Cfg::A_BYTES;
-        const uint32_t mcol = tmem + static_cast<uint32_t>(Cfg::META_COL0 + stage * Cfg::META_COLS);
-        const int64_t ks_left = (p.K - kb * Cfg::BK) / T::KSTEP;
-        const int ksteps = ks_left < Cfg::KSTEPS ? static_cast<int>(ks_left) : Cfg::KSTEPS;
+    // The whole warp runs the loop (warp-uniform addresses and descriptors);
+    // one elected lane issues the MMAs and commits.
+    int stage = 0;
+    uint32_t phase = 0;
+    const uint32_t smem0 = smem_u32(smem);
+    const int64_t k_last = p.K - (KI - 1) * Cfg::BK;   // whole K-steps in the last k-block (others: KSTEPS)
+    const int ksteps_last = k_last / T::KSTEP < Cfg::KSTEPS ? static_cast<int>(k_last / T::KSTEP) : Cfg::KSTEPS;
+    for (int64_t kb = kb0; kb < kb1; ++kb) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&meta_bar[stage]), phase, p.status) &&
+                                                  mbar_wait(smem_u32(&fulla_bar[stage]), phase, p.status) &&
+                                                  mbar_wait(smem_u32(&fullb_bar[stage]), phase, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t a0 = smem0 + static_cast<uint32_t>(stage * Cfg::STAGE_BYTES);
+      const uint64_t da = smem_desc(a0, 16, 1024, kSwizzle128B);
+      const uint64_t db = smem_desc(a0 + Cfg::A_BYTES, 16, 1024, kSwizzle128B);
+      const uint32_t mcol = tmem + static_cast<uint32_t>(Cfg::META_COL0 + stage * Cfg::META_COLS);
+      const int ksteps = kb == KI - 1 ? ksteps_last : Cfg::KSTEPS;
+      if (elect_one_lane()) {
 #pragma unroll
         for (int ks = 0; ks < Cfg::KSTEPS; ++ks) {
           if (ks >= ksteps) break;
-          const uint64_t da = smem_desc(a0 + (ks >> 2) * (Cfg::BM * 128) + (ks & 3) * 32, 16, 1024, kSwizzle128B);
-          const uint64_t db = smem_desc(b0 + (ks >> 1) * (BN * 128) + (ks & 1) * 64, 16, 1024, kSwizzle128B);
+          // descriptor start addresses advance in 16-byte units (no carry: shared memory < 256 KB)
+          const uint64_t dak = da + static_cast<uint64_t>(((ks >> 2) * (Cfg::BM * 128) + (ks & 3) * 32) >> 4);
+          const uint64_t dbk = db + static_cast<uint64_t>(((ks >> 1) * (BN * 128) + (ks & 1) * 64) >> 4);
           const uint32_t acc = (kb > kb0 || ks > 0) ? 1u : 0u;
           if constexpr (T::ES == 2)
-            tc_mma_sp_f16(tmem, da, db, mcol + 4 * ks, Cfg::IDESC, acc);
+            tc_mma_sp_f16(tmem, dak, dbk, mcol + 4 * ks, Cfg::IDESC, acc);
           else
-            tc_mma_sp_f8f6f4(tmem, da, db, mcol + 4 * ks, Cfg::IDESC, acc);
+            tc_mma_sp_f8f6f4(tmem, dak, dbk, mcol + 4 * ks, Cfg::IDESC, acc);
         }
         tc_commit(smem_u32(&empty_bar[stage]));
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
-      tc_commit(smem_u32(tfull_bar));
-      // Every tcgen05 operation of this thread has completed before TMEM is freed.
-      tc_commit(smem_u32(drain_bar));
-      mbar_wait(smem_u32(drain_bar), 0, p.status);
+      __syncwarp();
+      if (++stage == STAGES) { stage = 0; phase ^= 1u; }
     }
+    if (elect_one_lane()) {
+      tc_commit(smem_u32(tfull_bar));
+      // Every tcgen05 operation of this warp has completed before TMEM is freed.
+      tc_commit(smem_u32(drain_bar));
+    }
+    __syncwarp();
+    mbar_wait(smem_u32(drain_bar), 0, p.status);
   } else if (warp >= 6) {
     // ------------------------------------------------------------ metadata
     // Needs only the stage's values and metadata, not B: the stages loaded

@@ -160,39 +160,49 @@ __global__ void __launch_bounds__(448, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int abuf = 0;
-      uint32_t aphase = 0;
-      bool ok = true;
-      for (int64_t t = cta; ok && t < tiles; t += G) {
-        if (!mbar_wait(smem_u32(&tempty_bar[abuf]), aphase ^ 1u, p.status)) break;
+    // The whole warp runs the loop (warp-uniform addresses and descriptors);
+    // one elected lane issues the MMAs and commits.
+    int stage = 0;
+    uint32_t phase = 0;
+    int abuf = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    const uint32_t smem0 = smem_u32(smem);
+    for (int64_t t = cta; ok && t < tiles; t += G) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tempty_bar[abuf]), aphase ^ 1u, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d = tmem + static_cast<uint32_t>(abuf * BN);
+      for (int64_t mi = 0; mi < MI; ++mi) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&expd_bar[stage]), phase, p.status) &&
+                                         mbar_wait(smem_u32(&full_bar[stage]), phase, p.status));
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t d = tmem + static_cast<uint32_t>(abuf * BN);
-        for (int64_t mi = 0; mi < MI; ++mi) {
-          if (!mbar_wait(smem_u32(&expd_bar[stage]), phase, p.status) ||
-              !mbar_wait(smem_u32(&full_bar[stage]), phase, p.status)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t st = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+        const uint32_t st = smem0 + static_cast<uint32_t>(stage * Cfg::STAGE_BYTES);
+        const uint64_t da = smem_desc(st + Cfg::A_OFF, 8192, 1024, kSwizzle128B);
+        const uint64_t db = smem_desc(st + Cfg::B_OFF, 16, 1024, kSwizzle128B);
+        if (elect_one_lane()) {
 #pragma unroll
           for (int j = 0; j < Cfg::SM / 16; ++j) {
             // A: rows 16j..16j+15 of the dense tile (two 8-row groups, 1 KB apart),
             // the 128 k in two 64-element blocks 8 KB apart; B: 16 m-elements = 32 B.
-            const uint64_t da = smem_desc(st + Cfg::A_OFF + j * 2048, 8192, 1024, kSwizzle128B);
-            const uint64_t db = smem_desc(st + Cfg::B_OFF + j * 32, 16, 1024, kSwizzle128B);
-            tc_mma_f16(d, da, db, Cfg::IDESC, (mi > 0 || j > 0) ? 1u : 0u);
+            // Start addresses advance in 16-byte units (no carry: shared memory < 256 KB).
+            tc_mma_f16(d, da + static_cast<uint64_t>(j * (2048 >> 4)), db + static_cast<uint64_t>(j * (32 >> 4)),
+                       Cfg::IDESC, (mi > 0 || j > 0) ? 1u : 0u);
           }
           tc_commit(smem_u32(&empty_bar[stage]));
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        if (!ok) break;
-        tc_commit(smem_u32(&tfull_bar[abuf]));
-        if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
-      tc_commit(smem_u32(drain_bar));
-      mbar_wait(smem_u32(drain_bar), 0, p.status);
+      if (!ok) break;
+      if (elect_one_lane()) tc_commit(smem_u32(&tfull_bar[abuf]));
+      __syncwarp();
+      if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
     }
+    if (elect_one_lane()) tc_commit(smem_u32(drain_bar));
+    __syncwarp();
+    mbar_wait(smem_u32(drain_bar), 0, p.status);
   } else if (warp >= 6) {
     // ------------------------------------------------------------ expansion
     // Thread e: row r = e / 4 of the stage, chunks c = 4q..4q+3 (q = e % 4),

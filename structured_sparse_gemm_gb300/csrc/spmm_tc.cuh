@@ -238,50 +238,61 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int abuf = 0;
-      uint32_t aphase = 0;
-      bool ok = true;
-      Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, cta);
-      Segment sg;
-      while (ok && sch.next(sg)) {
-        const int64_t kb0 = sg.kb0, kb1 = sg.kb1;
-        if (!mbar_wait(smem_u32(&tempty_bar[abuf]), aphase ^ 1u, p.status)) { ok = false; break; }
+    // The whole warp runs the loop (its addresses and descriptors stay
+    // warp-uniform); one elected lane issues the MMAs and commits.
+    int stage = 0;
+    uint32_t phase = 0;
+    int abuf = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    const uint32_t smem0 = smem_u32(smem);
+    const int64_t k_last = p.K - (KI - 1) * T::BK;   // whole K-steps in the last k-block (others: 4)
+    const int ksteps_last = k_last / T::KSTEP < 4 ? static_cast<int>(k_last / T::KSTEP) : 4;
+    Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, cta);
+    Segment sg;
+    while (ok && sch.next(sg)) {
+      const int64_t kb0 = sg.kb0, kb1 = sg.kb1;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tempty_bar[abuf]), aphase ^ 1u, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d = tmem + static_cast<uint32_t>(abuf * BN);
+      for (int64_t kb = kb0; kb < kb1; ++kb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&meta_bar[stage]), phase, p.status) &&
+                                         mbar_wait(smem_u32(&full_bar[stage]), phase, p.status));
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t d = tmem + static_cast<uint32_t>(abuf * BN);
-        for (int64_t kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(smem_u32(&meta_bar[stage]), phase, p.status) ||
-              !mbar_wait(smem_u32(&full_bar[stage]), phase, p.status)) { ok = false; break; }
-          tc_fence_after();
-          uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
-          const uint32_t mcol = tmem + static_cast<uint32_t>(Cfg::META_COL0 + stage * T::META_COLS);
-          const int64_t ks_left = (p.K - kb * T::BK) / T::KSTEP;
-          const int ksteps = ks_left < 4 ? static_cast<int>(ks_left) : 4;
-          const uint32_t a0 = smem_u32(st), b0 = smem_u32(st + Cfg::A_BYTES);
+        const uint32_t a0 = smem0 + static_cast<uint32_t>(stage * Cfg::STAGE_BYTES);
+        const uint64_t da = smem_desc(a0, 16, 1024, kSwizzle128B);
+        const uint64_t db = smem_desc(a0 + Cfg::A_BYTES, 16, 1024, kSwizzle128B);
+        const uint32_t mcol = tmem + static_cast<uint32_t>(Cfg::META_COL0 + stage * T::META_COLS);
+        const int ksteps = kb == KI - 1 ? ksteps_last : 4;
+        if (elect_one_lane()) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             if (ks >= ksteps) break;
-            const uint64_t da = smem_desc(a0 + ks * 32, 16, 1024, kSwizzle128B);
-            const uint64_t db = smem_desc(b0 + (ks >> 1) * (BN * 128) + (ks & 1) * 64, 16, 1024, kSwizzle128B);
+            // descriptor start addresses advance in 16-byte units (no carry: shared memory < 256 KB)
+            const uint64_t dak = da + static_cast<uint64_t>(ks * 2);
+            const uint64_t dbk = db + static_cast<uint64_t>(((ks >> 1) * (BN * 128) + (ks & 1) * 64) >> 4);
             const uint32_t acc = (kb > kb0 || ks > 0) ? 1u : 0u;
             if constexpr (T::ES == 2)
-              tc_mma_sp_f16(d, da, db, mcol + 4 * ks, Cfg::IDESC, acc);
+              tc_mma_sp_f16(d, dak, dbk, mcol + 4 * ks, Cfg::IDESC, acc);
             else
-              tc_mma_sp_f8f6f4(d, da, db, mcol + 4 * ks, Cfg::IDESC, acc);
+              tc_mma_sp_f8f6f4(d, dak, dbk, mcol + 4 * ks, Cfg::IDESC, acc);
           }
           tc_commit(smem_u32(&empty_bar[stage]));
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        if (!ok) break;
-        tc_commit(smem_u32(&tfull_bar[abuf]));
-        if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
-      // Every tcgen05 operation of this thread has completed before TMEM is freed.
-      tc_commit(smem_u32(drain_bar));
-      mbar_wait(smem_u32(drain_bar), 0, p.status);
+      if (!ok) break;
+      if (elect_one_lane()) tc_commit(smem_u32(&tfull_bar[abuf]));
+      __syncwarp();
+      if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
     }
+    // Every tcgen05 operation of this warp has completed before TMEM is freed.
+    if (elect_one_lane()) tc_commit(smem_u32(drain_bar));
+    __syncwarp();
+    mbar_wait(smem_u32(drain_bar), 0, p.status);
   } else if (warp >= 6) {
     // ------------------------------------------------------------ metadata
     const int q = warp & 3;                 // TMEM lane quadrant of this warp
@@ -356,12 +367,20 @@ __global__ void __launch_bounds__(320, 1)
           constexpr int CT = decltype(ct)::value;
 #pragma unroll 1
           for (int c = 0; c < BN; c += CH) {
-            float bc[CH];
-            if (row_ok && p.beta != 0.0f) load_row_chunk_beta_c<CT, CH>(p, m, n_base + c, bc);
             uint32_t r[CH];
             if constexpr (CH == 32) tmem_ld_x32(tacc + c, r); else tmem_ld_x16(tacc + c, r);
             tmem_ld_wait();
-            if (row_ok) store_row_chunk_bits<CT, CH>(p, m, n_base + c, r, bc, f);
+            if (row_ok) {
+#pragma unroll
+              for (int g = 0; g < CH; g += 8) {   // 8 columns at a time: few registers live
+                float bc[8];
+                uint32_t rg[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) rg[j] = r[g + j];
+                if (p.beta != 0.0f) load_row_chunk_beta_c<CT, 8>(p, m, n_base + c + g, bc);
+                store_row_chunk_bits<CT, 8>(p, m, n_base + c + g, rg, bc, f);
+              }
+            }
           }
         });
         tc_fence_before();
@@ -394,7 +413,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         named_barrier_sync(1, 128);
         if (*s_last && row_ok)
-          reduce_split_row<Cfg::BM, BN, (BN < 16 ? BN : 16)>(p, p.partials, sch, tile, 1, 0, c_lo, c_hi,
+          reduce_split_row<Cfg::BM, BN, (BN < 8 ? BN : 8)>(p, p.partials, sch, tile, 1, 0, c_lo, c_hi,
                                                              32 * q + lane, m, n_base, f);
       }
       if (++abuf == 2) { abuf = 0; aphase ^= 1u; }

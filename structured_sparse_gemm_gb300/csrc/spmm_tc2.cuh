@@ -41,6 +41,14 @@
 namespace st24 {
 namespace tc2 {
 
+// One staged C value (output type CT) at a 32-bit shared address, as fp32.
+template <int CT>
+__device__ __forceinline__ float staged_c(uint32_t at) {
+  if constexpr (CT == kF32) return lds_f32(at);
+  else if constexpr (CT == kBF16) return __uint_as_float(lds_u16(at) << 16);
+  else return __half2float(__ushort_as_half(static_cast<unsigned short>(lds_u16(at))));
+}
+
 using tc::TcParams;
 using tc::TcTraits;
 
@@ -399,20 +407,19 @@ __global__ void __launch_bounds__(320, 1)
             if (n_base + c >= p.N) continue;   // warp-uniform: nothing of this chunk is in the output
             const int b = (c / CH) & 1;
             const uint32_t buf = smem_u32(my_cbuf + b * Cfg::CBUF_BYTES);
-            float bc[CH];
             if (stage_c) {
               mbar_wait(smem_u32(&my_cbar[b]), cpar[b], p.status);
               cpar[b] ^= 1u;
-              staged_beta_c<CT, CH>(buf, lane, p.beta, bc);   // each lane then overwrites only what it read
             } else {
               if (lane == 0) bulk_wait_read<1>();   // the store of two chunks ago has read this buffer
               __syncwarp();
             }
+            // each lane overwrites in place only the staged values it read
 #pragma unroll
             for (int j = 0; j < CH; ++j) {
               float o = __fmul_rn(__uint_as_float(r[j]), f);
-              if (p.beta != 0.0f) o = __fadd_rn(o, bc[j]);
               const uint32_t at = buf + (j * 32 + lane) * CS;
+              if (p.beta != 0.0f) o = __fadd_rn(o, __fmul_rn(p.beta, staged_c<CT>(at)));
               if constexpr (CT == kF32) sts_f32(at, o);
               else if constexpr (CT == kBF16) sts_u16(at, __bfloat16_as_ushort(__float2bfloat16_rn(o)));
               else sts_u16(at, __half_as_ushort(__float2half_rn(o)));
@@ -431,12 +438,20 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll 1
           for (int c = 0; c < BNP; c += CH) {
             const bool live = row_ok && n_base + c < p.N;
-            float bc[CH];
-            if (live && p.beta != 0.0f) load_row_chunk_beta_c<CT, CH>(p, m, n_base + c, bc);
             uint32_t r[CH];
             tmem_ld_x32(tacc + c, r);
             tmem_ld_wait();
-            if (live) store_row_chunk_bits<CT, CH>(p, m, n_base + c, r, bc, f);
+            if (live) {
+#pragma unroll
+              for (int g = 0; g < CH; g += 8) {   // 8 columns at a time: few registers live
+                float bc[8];
+                uint32_t rg[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) rg[j] = r[g + j];
+                if (p.beta != 0.0f) load_row_chunk_beta_c<CT, 8>(p, m, n_base + c + g, bc);
+                store_row_chunk_bits<CT, 8>(p, m, n_base + c + g, rg, bc, f);
+              }
+            }
           }
         });
       }
@@ -473,7 +488,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         named_barrier_sync(1, 128);
         if (*s_last && row_ok)
-          reduce_split_row<Cfg::BM, BNP, 16>(p, p.partials, sch, tile, 2, static_cast<int>(rank), c_lo, c_hi,
+          reduce_split_row<Cfg::BM, BNP, 8>(p, p.partials, sch, tile, 2, static_cast<int>(rank), c_lo, c_hi,
                                              32 * q + lane, m, n_base, f);
       }
       if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
