@@ -572,12 +572,16 @@ st24_status launch_pair(const SpmmArgs& a, const StreamKPlan& plan, const Device
   p.k_iters = plan.k_iters;
   p.dp_tiles = plan.dp_tiles;
   p.sk_tiles = plan.sk_tiles;
-  // A is streamed through L2 only when a single tile column reads it; B
-  // stays (it is re-read by every m-tile group).  Marking the operand the
-  // raster streams as evict-first was measured: it raised DRAM re-reads when
-  // the output stream (C) competes for L2.
+  // L2 policy per operand.  A is streamed once when a single tile column
+  // reads it.  When the raster keeps the whole A resident (one group of all
+  // m-tiles, n-tiles outer), each B panel is read by the m-tiles of one wave
+  // and never again: evict-first, so that the panels passing through do not
+  // push A out (measured on 4096x11008, N = 4096: DRAM reads 355 -> 240 MB,
+  // same time).  Otherwise B stays: it is re-read by every m-tile group.
+  // (Marking A evict-first in the row-major raster was measured to raise
+  // DRAM re-reads when the output stream C competes for L2.)
   p.a_evict_first = plan.tiles_n == 1 ? 1 : 0;
-  p.b_evict_first = 0;
+  p.b_evict_first = (plan.group_m >= plan.tiles_m && plan.tiles_m > 1 && plan.tiles_n > 1) ? 1 : 0;
   p.a_fixed = (a.flags & ST24_SPMM_FIXED_A) ? 1 : 0;
   p.partials = static_cast<float*>(a.workspace);
   p.counters = plan.ws_bytes ? reinterpret_cast<unsigned*>(static_cast<uint8_t*>(a.workspace) +
