@@ -29,10 +29,37 @@ StreamKPlan plan_spmm_tc(const SpmmArgs& a, int num_sms) {
   const int bn = pick_bn_tc(a.N);
   if (bn < 128) return make_stream_k_plan(128, bn, bk, a.M, a.N, a.K, num_sms, a_row, b_col, false);
   // Wide N: M = 256 tiles on CTA pairs, scheduled over num_sms / 2 pairs.
+  // Costs in k-blocks of MMA time per pair.  Whole tiles in data-parallel
+  // waves cost waves * k_iters.  Splitting a tile s ways over K costs
+  // k_iters / s plus finishing it: the partials go through the workspace and
+  // the last contributor sums them, about 50 + 23 s k-blocks (measured).  So
+  // tiles are split only when they are fewer than the pairs and long: a
+  // stream-K tail after full waves never pays (11008x4096 at N = 600, 1000
+  // and 2048 and 4096x4096 at N = 2048 ran 1.7-2.6x faster as data-parallel
+  // waves), nor does a split over all the pairs (256x32768 at N = 200 took 8x
+  // the unsplit time split 76 ways).
+  const int pairs = num_sms / 2;
+  const int bnp = pick_bnp(a.N);
+  const int64_t tiles = ((a.M + 255) / 256) * ((a.N + bnp - 1) / bnp);
+  const int64_t KI = (a.K + bk - 1) / bk;
+  double best = static_cast<double>((tiles + pairs - 1) / (pairs > 0 ? pairs : 1)) * static_cast<double>(KI);
+  int64_t best_s = 1;
+  for (int64_t sp = 2; tiles > 0 && sp * tiles <= pairs; ++sp) {
+    const double cost = static_cast<double>(KI) / sp + 50.0 + 23.0 * sp;
+    if (cost < best) { best = cost; best_s = sp; }
+  }
+  // A grid of tiles * best_s pairs: every tile split best_s ways (whole
+  // tiles when best_s is 1), each pair taking one contiguous run of k-blocks.
+  const int64_t g = best_s > 1 ? tiles * best_s : (tiles < pairs ? (tiles > 0 ? tiles : 1) : pairs);
+  StreamKPlan pl = make_stream_k_plan(256, bnp, bk, a.M, a.N, a.K, static_cast<int>(g), a_row, b_col, false);
+  pl.pair = 1;
+  if (best_s == 1 && tiles > pl.grid) {   // full waves: never a stream-K tail
+    pl.dp_tiles = tiles;
+    pl.sk_tiles = 0;
+    pl.ws_bytes = 0;
+  }
   // Each CTA keeps its own partial tile and counter, so a pair needs two
   // counters per tile.
-  StreamKPlan pl = make_stream_k_plan(256, pick_bnp(a.N), bk, a.M, a.N, a.K, num_sms / 2, a_row, b_col, false);
-  pl.pair = 1;
   if (pl.ws_bytes > 0)
     pl.ws_bytes = 2 * static_cast<size_t>(pl.grid) * pl.partial_bytes +
                   (static_cast<size_t>(pl.tiles_m * pl.tiles_n) * 2 * 4 + 255) / 256 * 256;

@@ -310,3 +310,13 @@ def test_fp8_sampled_mma_sp(N):
 @pytest.mark.slow
 def test_prefill_bf16_sampled_mma_sp():
     check_sampled(inputs.prefill_bf16(4096, 11008), count=512, kernel="mma_sp")
+
+
+# Few, long output tiles: the CTA pairs split them over K and finish them
+# through the workspace (the last contributor sums the partials); more tiles
+# run as whole tiles in data-parallel waves.  Both schedules, with beta.
+@pytest.mark.parametrize("ab", ["bf16", "e4m3"])
+@pytest.mark.parametrize("M,N,K", [(256, 200, 32768), (512, 448, 16384), (1024, 1000, 2048)])
+def test_pair_schedules(ab, M, N, K):
+    case = inputs.spmm_case(ab, "bf16", M, N, K, a_std=0.02 if ab == "e4m3" else 1.0, seed=M + N, beta=0.5)
+    check_sampled(case, count=1024, kernel="tcgen05")
