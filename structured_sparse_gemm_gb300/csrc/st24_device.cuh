@@ -387,6 +387,18 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d, uint64_t a, uint64_t b, u
       : "memory");
 }
 
+// The dense MMA on a CTA pair: M = 256, A rows 0-127 and D rows 0-127 in the
+// issuing CTA, rows 128-255 in its peer (same shared-memory and TMEM
+// addresses); B's N rows split in halves the same way.
+__device__ __forceinline__ void tc_mma_f16_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A(smem, 2:4 sparse, metadata in tmem) * B(smem).
 __device__ __forceinline__ void tc_mma_sp_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t meta,
                                               uint32_t idesc, uint32_t accumulate) {
