@@ -746,6 +746,65 @@ def measure(name, args, rank, world, target_s, cpu_budget_s):
     return rec
 
 
+# Small cases that launch one kernel family a few times and exit: what the
+# profiler captures (the last launches are the steady-state ones).
+KERNEL_CASES = {
+    "fp8_pair": "st24_spmm e4m3 28672x8192, N = 4096, one weight: 3 launches of the CTA-pair kernel",
+    "prefill_pair": "st24_spmm bf16 11008x4096 and 4096x11008, N = 4096, beta = 1: 3 launches of each, alternating",
+    "transposed_pair": "st24_spmm_t bf16 11008x4096 weight, N = 4096, beta = 1: 3 launches of the CTA-pair kernel",
+    "decode_narrow": "st24_spmm bf16 4096x4096, N = 16, 4 weights: 2 rounds of 4 launches of the narrow kernel",
+    "prune_bf16": "st24_prune_compress and st24_prune_compress_nm2 (4:8) of a bf16 28672x8192 weight: twice each",
+}
+
+
+def run_kernel_case(name):
+    import structured_sparse_gemm_gb300 as st
+    dev = torch.device("cuda", 0)
+    st.load()
+    g = inputs.generator(0)
+
+    def compressed(ab, M, K):
+        W = inputs.draw(ab, (M, K), 0.02, g).to(dev)
+        v = torch.empty((M, K // 2), dtype=W.dtype, device=dev)
+        m = torch.empty((M, K // 8), dtype=torch.uint8, device=dev)
+        st.st24_prune_compress(W, v, m)
+        return v, m
+
+    def product(ab, M, K, N, beta):
+        v, m = compressed(ab, M, K)
+        X = inputs.draw(ab, (N, K), 1.0, g).to(dev)
+        Y = inputs.draw("bf16", (N, M), 1.0, g).to(dev)
+        ws = torch.zeros(max(st.st24_spmm_workspace_bytes(ab, "bf16", M, N, K), 16), dtype=torch.uint8, device=dev)
+        return lambda: st.st24_spmm(v, m, X, Y, K=K, beta=beta, workspace=ws, fixed_a=True)
+
+    if name == "fp8_pair":
+        calls = [product("e4m3", 28672, 8192, 4096, 0.0)] * 3
+    elif name == "prefill_pair":
+        a, b = product("bf16", 11008, 4096, 4096, 1.0), product("bf16", 4096, 11008, 4096, 1.0)
+        calls = [a, b] * 3
+    elif name == "transposed_pair":
+        v, m = compressed("bf16", 11008, 4096)
+        dY = inputs.draw("bf16", (4096, 11008), 1.0, g).to(dev)
+        dX = inputs.draw("bf16", (4096, 4096), 1.0, g).to(dev)
+        calls = [lambda: st.st24_spmm_t(v, m, dY, dX, K=4096, beta=1.0)] * 3
+    elif name == "decode_narrow":
+        calls = [product("bf16", 4096, 4096, 16, 0.0) for _ in range(4)] * 2
+    else:   # prune_bf16
+        W = inputs.prune_weight_bf16().to(dev)
+        M, K = W.shape
+        v = torch.empty((M, K // 2), dtype=W.dtype, device=dev)
+        m = torch.empty((M, K // 8), dtype=torch.uint8, device=dev)
+        v2 = torch.empty((M, K), dtype=W.dtype, device=dev)
+        m2 = torch.empty((M, K // 4), dtype=torch.uint8, device=dev)
+        calls = [lambda: st.st24_prune_compress(W, v, m), lambda: st.st24_prune_compress_nm2(W, v2, m2, 4, 8)] * 2
+    torch.cuda.synchronize()
+    for c in calls:
+        c()
+    torch.cuda.synchronize()
+    if st.st24_device_status() != 0:
+        raise RuntimeError("device status set")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -765,7 +824,12 @@ def main():
                     help="SpMM kernel family (auto = what st24_spmm picks)")
     ap.add_argument("--no-fixed-a", dest="fixed_a", action="store_false",
                     help="do not declare the weights fixed (ST24_SPMM_FIXED_A) to the products")
+    ap.add_argument("--kernel-case", choices=sorted(KERNEL_CASES),
+                    help="run one small profiling case (a few launches of one kernel family) and exit")
     args = ap.parse_args()
+    if args.kernel_case:
+        run_kernel_case(args.kernel_case)
+        return
     head = HEADLINE if args.workload == "all" else args.workload
     subs = SUB_WORKLOADS if args.workload == "all" else []
     w = WORKLOADS[head]
