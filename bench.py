@@ -754,6 +754,11 @@ KERNEL_CASES = {
     "transposed_pair": "st24_spmm_t bf16 11008x4096 weight, N = 4096, beta = 1: 3 launches of the CTA-pair kernel",
     "decode_narrow": "st24_spmm bf16 4096x4096, N = 16, 4 weights: 2 rounds of 4 launches of the narrow kernel",
     "prune_bf16": "st24_prune_compress and st24_prune_compress_nm2 (4:8) of a bf16 28672x8192 weight: twice each",
+    "fp8_groups": "st24_spmm e4m3 28672x8192 at N = 512, 4096 and 8192 (the tensor-bound groups), one weight: two rounds",
+    "decode_mix": "st24_spmm bf16 4096x4096 at N = 1, 16 and 32, one weight each: two rounds",
+    "int8_mix": "st24_spmm int8 8192x8192 at N = 16 and 2048, row scales, bf16 out: two rounds",
+    "demo_pair": "st24_spmm bf16 4096x4096, N = 4096: 3 launches",
+    "transposed_both": "st24_spmm_t bf16 11008x4096 and 4096x11008 weights, N = 4096: two rounds",
 }
 
 
@@ -770,12 +775,19 @@ def run_kernel_case(name):
         st.st24_prune_compress(W, v, m)
         return v, m
 
-    def product(ab, M, K, N, beta):
-        v, m = compressed(ab, M, K)
+    def product(ab, M, K, N, beta, vm=None):
+        v, m = vm if vm is not None else compressed(ab, M, K)
         X = inputs.draw(ab, (N, K), 1.0, g).to(dev)
         Y = inputs.draw("bf16", (N, M), 1.0, g).to(dev)
+        scale = inputs.row_scale(M, g).to(dev) if ab == "s8" else None
         ws = torch.zeros(max(st.st24_spmm_workspace_bytes(ab, "bf16", M, N, K), 16), dtype=torch.uint8, device=dev)
-        return lambda: st.st24_spmm(v, m, X, Y, K=K, beta=beta, workspace=ws, fixed_a=True)
+        return lambda: st.st24_spmm(v, m, X, Y, K=K, beta=beta, row_scale=scale, workspace=ws, fixed_a=True)
+
+    def transposed(M, K, N):
+        v, m = compressed("bf16", M, K)
+        dY = inputs.draw("bf16", (N, M), 1.0, g).to(dev)
+        dX = inputs.draw("bf16", (N, K), 1.0, g).to(dev)
+        return lambda: st.st24_spmm_t(v, m, dY, dX, K=K, beta=1.0)
 
     if name == "fp8_pair":
         calls = [product("e4m3", 28672, 8192, 4096, 0.0)] * 3
@@ -783,12 +795,21 @@ def run_kernel_case(name):
         a, b = product("bf16", 11008, 4096, 4096, 1.0), product("bf16", 4096, 11008, 4096, 1.0)
         calls = [a, b] * 3
     elif name == "transposed_pair":
-        v, m = compressed("bf16", 11008, 4096)
-        dY = inputs.draw("bf16", (4096, 11008), 1.0, g).to(dev)
-        dX = inputs.draw("bf16", (4096, 4096), 1.0, g).to(dev)
-        calls = [lambda: st.st24_spmm_t(v, m, dY, dX, K=4096, beta=1.0)] * 3
+        calls = [transposed(11008, 4096, 4096)] * 3
+    elif name == "transposed_both":
+        calls = [transposed(11008, 4096, 4096), transposed(4096, 11008, 4096)] * 2
     elif name == "decode_narrow":
         calls = [product("bf16", 4096, 4096, 16, 0.0) for _ in range(4)] * 2
+    elif name == "decode_mix":
+        calls = [product("bf16", 4096, 4096, n, 0.0) for n in (1, 16, 32)] * 2
+    elif name == "fp8_groups":
+        vm = compressed("e4m3", 28672, 8192)
+        calls = [product("e4m3", 28672, 8192, n, 0.0, vm) for n in (512, 4096, 8192)] * 2
+    elif name == "int8_mix":
+        vm = compressed("s8", 8192, 8192)
+        calls = [product("s8", 8192, 8192, n, 0.0, vm) for n in (16, 2048)] * 2
+    elif name == "demo_pair":
+        calls = [product("bf16", 4096, 4096, 4096, 0.0)] * 3
     else:   # prune_bf16
         W = inputs.prune_weight_bf16().to(dev)
         M, K = W.shape
