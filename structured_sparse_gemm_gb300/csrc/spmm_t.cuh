@@ -43,7 +43,7 @@ struct Config {
   static constexpr int STAGES = STAGES_;
   static constexpr int THREADS = 448;
   static constexpr int EXPAND_THREADS = 256;
-  static constexpr int V_BYTES = SM * 128;       // compressed values: [64 rows][64 values]
+  static constexpr int V_BYTES = SM * 128;       // compressed values: [64 rows][128 B], 128-byte swizzle
   static constexpr int E_BYTES = SM * 16;        // metadata: [64 rows][16 B]
   static constexpr int B_BYTES = BN * 128;       // dY: [BN rows][64 m-elements], 128-byte swizzle
   static constexpr int A_BYTES = SM * BM * 2;    // dense tile: [2 k-blocks][8 m-groups][8 rows][128 B]
@@ -60,6 +60,7 @@ struct Config {
   static constexpr uint32_t IDESC = (1u << 4) | (FMT << 7) | (FMT << 10) | (1u << 15) |
                                     (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "N of the MMA");
+  static_assert(V_OFF % 1024 == 0, "128-byte swizzle atoms of the values");
   static_assert(TMEM_COLS <= 512, "tensor memory");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
   static_assert((4 * STAGES + 5) * 8 + 8 <= 256, "barrier region");
@@ -205,10 +206,13 @@ __global__ void __launch_bounds__(448, 1)
     mbar_wait(smem_u32(drain_bar), 0, p.status);
   } else if (warp >= 6) {
     // ------------------------------------------------------------ expansion
-    // Thread e: row r = e / 4 of the stage, chunks c = 4q..4q+3 (q = e % 4),
-    // chunk c = the 8 k of groups 2c, 2c+1 = one 16-byte run of the dense row.
+    // Thread e: row r of the stage, chunks c = 4q..4q+3, chunk c = the 8 k of
+    // groups 2c, 2c+1 = one 16-byte run of the dense row.  The 8 lanes of each
+    // quarter-warp take 8 consecutive rows with the same q, so that their
+    // 16-byte reads (values stored with the 128-byte swizzle) and writes (the
+    // dense tile's swizzle) fall in 8 different bank quads.
     const int e = threadIdx.x - 192;
-    const int r = e >> 2, q = e & 3;
+    const int r = ((e >> 5) << 3) | (e & 7), q = (e >> 3) & 3;
     const int g = r >> 3, rr = r & 7;
     int stage = 0;
     uint32_t phase = 0;
@@ -217,8 +221,8 @@ __global__ void __launch_bounds__(448, 1)
       for (int64_t mi = 0; mi < MI; ++mi) {
         if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.status)) { ok = false; break; }
         uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
-        const uint4 v0 = *reinterpret_cast<const uint4*>(st + Cfg::V_OFF + r * 128 + q * 32);
-        const uint4 v1 = *reinterpret_cast<const uint4*>(st + Cfg::V_OFF + r * 128 + q * 32 + 16);
+        const uint4 v0 = *reinterpret_cast<const uint4*>(st + Cfg::V_OFF + r * 128 + (((2 * q) ^ rr) << 4));
+        const uint4 v1 = *reinterpret_cast<const uint4*>(st + Cfg::V_OFF + r * 128 + (((2 * q + 1) ^ rr) << 4));
         const uint32_t mb = *reinterpret_cast<const uint32_t*>(st + Cfg::E_OFF + r * 16 + q * 4);
         const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll

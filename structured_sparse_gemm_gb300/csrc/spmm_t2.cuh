@@ -53,7 +53,7 @@ struct Config {
   static constexpr int STAGES = OPS_;            // operand ring
   static constexpr int VES = VES_;               // compressed-tile ring
   static constexpr int THREADS = 480;
-  static constexpr int V_BYTES = SM * 128;       // compressed values: [64 rows][64 values]
+  static constexpr int V_BYTES = SM * 128;       // compressed values: [64 rows][128 B], 128-byte swizzle
   static constexpr int E_BYTES = SM * 16;        // metadata: [64 rows][16 B]
   static constexpr int B_BYTES = BH * 128;       // this CTA's half of dY: [BH rows][64 m], 128-byte swizzle
   static constexpr int A_BYTES = SM * BM * 2;    // dense tile: [2 k-blocks][8 m-groups][8 rows][128 B]
@@ -75,6 +75,7 @@ struct Config {
   static constexpr uint32_t IDESC = (1u << 4) | (FMT << 7) | (FMT << 10) | (1u << 15) |
                                     (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "N of the pair MMA; dY halves of whole 16-row blocks");
+  static_assert(VE_BASE % 1024 == 0 && VE_STAGE_BYTES % 1024 == 0, "128-byte swizzle atoms of the values");
   static_assert(TMEM_COLS <= 512, "tensor memory");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
   static_assert(VES >= STAGES && VES <= 32, "compressed ring at least as deep as the operand ring");
@@ -263,13 +264,16 @@ __global__ void __launch_bounds__(480, 1)
     // Two groups of 4 warps take alternate stages (group 0 the even ones of
     // this CTA's sequence), so that two stages expand at once: a stage's
     // expansion is a chain of dependent shared-memory steps, and one group
-    // alone left the MMA waiting on it.  Thread e of a group: row r = e / 2 of
-    // the stage, chunks c = 8h..8h+7 (h = e % 2), chunk c = the 8 k of groups
-    // 2c, 2c+1 = one 16-byte run of the dense row.
+    // alone left the MMA waiting on it.  Thread e of a group: row r of the
+    // stage, chunks c = 8h..8h+7, chunk c = the 8 k of groups 2c, 2c+1 = one
+    // 16-byte run of the dense row.  The 8 lanes of each quarter-warp take 8
+    // consecutive rows with the same h, so that their 16-byte reads (values
+    // stored with the 128-byte swizzle) and writes (the dense tile's swizzle)
+    // fall in 8 different bank quads.
     const int ew = warp - 6;                     // expansion warp 0-7
     const int grp = ew >> 2;
     const int e = (threadIdx.x - 192) & 127;
-    const int r = e >> 1, h = e & 1;
+    const int r = ((e >> 4) << 3) | (e & 7), h = (e >> 3) & 1;
     const int g = r >> 3, rr = r & 7;
     int stage = 0, vs = 0;
     uint32_t phase = 0, vph = 0;
@@ -286,7 +290,7 @@ __global__ void __launch_bounds__(480, 1)
           uint32_t vw[16];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const uint4 v = *reinterpret_cast<const uint4*>(sv + Cfg::V_OFF + r * 128 + h * 64 + 16 * u);
+            const uint4 v = *reinterpret_cast<const uint4*>(sv + Cfg::V_OFF + r * 128 + (((4 * h + u) ^ rr) << 4));
             vw[4 * u] = v.x; vw[4 * u + 1] = v.y; vw[4 * u + 2] = v.z; vw[4 * u + 3] = v.w;
           }
           const uint2 mb = *reinterpret_cast<const uint2*>(sv + Cfg::E_OFF + r * 16 + h * 8);

@@ -13,8 +13,11 @@ st24_status launch_cfg(const SpmmArgs& a, const DeviceInfo& dev, cudaStream_t st
   // A's values (K/2 per row) and metadata (K/8 bytes per row); dY as (M, N) with M inner.
   CUtensorMap tmV, tmE, tmB;
   const uint64_t kc = a.K / 2;
+  // Values with the 128-byte swizzle: the expansion threads of one 8-lane
+  // phase read the same 16-byte column of 8 consecutive rows, which the
+  // swizzle spreads over all 32 banks.
   if (!encode_tensor_map_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.values, kc, a.M, kc * 2, 64, Cfg::SM,
-                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tensor_map_2d(&tmE, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.meta, a.K / 8, a.M, a.K / 8, 16, Cfg::SM,
                             CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !encode_tensor_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.B, a.M, a.N, a.ldb * 2, 64, BN,
@@ -62,8 +65,11 @@ st24_status launch_pair(const SpmmArgs& a, const DeviceInfo& dev, cudaStream_t s
   using Cfg = spt2::Config<DT, BN, STAGES, VES>;
   CUtensorMap tmV, tmE, tmB;
   const uint64_t kc = a.K / 2;
+  // Values with the 128-byte swizzle: the expansion threads of one 8-lane
+  // phase read the same 16-byte column of 8 consecutive rows, which the
+  // swizzle spreads over all 32 banks.
   if (!encode_tensor_map_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.values, kc, a.M, kc * 2, 64, Cfg::SM,
-                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tensor_map_2d(&tmE, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.meta, a.K / 8, a.M, a.K / 8, 16, Cfg::SM,
                             CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !encode_tensor_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.B, a.M, a.N, a.ldb * 2, 64, Cfg::BH,
