@@ -511,6 +511,7 @@ st24_status launch_dt_impl(const SpmmArgs& a, const StreamKPlan& plan, const Dev
   constexpr bool k16 = TcTraits<DT>::ES == 2;
   if (plan.pair) {
     if (plan.bn == 128) return tc2::launch_pair<DT, 128, 5>(a, plan, dev, s);
+    if (plan.bn == 256) return tc2::launch_pair<DT, 256, 3>(a, plan, dev, s);
     return tc2::launch_pair<DT, 224, 4>(a, plan, dev, s);
   }
   switch (plan.bn) {

@@ -9,13 +9,17 @@
 // element against a one-CTA tile of the same N, which is what bounds the wide
 // products: the pipeline's bytes in flight per SM against L2 latency.
 //
-// Roles (320 threads per CTA, both CTAs):
-//  * warp 0, TMA producer: per stage, first its CTA's metadata (on its own
-//    metadata barrier), then its 128 rows of compressed A and its BNP / 2 rows
-//    of B.  The A and B loads of both CTAs complete on the leader's full
-//    barrier (the cta_group::2 form of the tensor load), which the leader's
-//    producer arms for the bytes of both; each CTA refills a stage when its
-//    own empty barrier (the MMA commit, multicast) says it is free.
+// Roles (352 threads per CTA, both CTAs):
+//  * warp 0, weight producer: per stage, first its CTA's metadata (on its own
+//    metadata barrier), then its 128 rows of compressed A; warp 10, B
+//    producer: its BNP / 2 rows of B.  The A and B loads of both CTAs complete
+//    on the leader's full barrier (the cta_group::2 form of the tensor load),
+//    which the leader's weight producer arms for the bytes of both; each CTA
+//    refills a stage when its own empty barrier (the MMA commit, multicast)
+//    says it is free.  Two issuing threads, because one thread issues tensor
+//    loads at a bounded rate (~90 cycles per box plus ~1 cycle per 117 bytes,
+//    measured): metadata, A and the two B boxes of a stage from one thread
+//    took ~800 cycles against ~450 of MMA work.
 //  * warps 6-9, metadata: once this CTA's metadata has landed, shared memory
 //    -> this CTA's TMEM (as in the one-CTA kernel), then signal the leader
 //    CTA's meta barrier: the leader's warps arrive on it (4 arrivals, each
@@ -59,14 +63,17 @@ struct PairConfig {
   static constexpr int BNP = BNP_;                   // N of the pair tile
   static constexpr int BH = BNP / 2;                 // rows of B staged per CTA
   static constexpr int STAGES = STAGES_;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 352;
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BH * 256;           // two 128-byte-wide boxes of BH rows
   static constexpr int E_BYTES = BM * T::EB;
   static constexpr int STAGE_TX = A_BYTES + B_BYTES + E_BYTES;
   static constexpr int PAIR_TX = 2 * (A_BYTES + B_BYTES);   // operand bytes of both CTAs per stage
   static constexpr int STAGE_BYTES = (STAGE_TX + 1023) / 1024 * 1024;
-  static constexpr int META_COL0 = 2 * BNP;          // after the two accumulators
+  // Two accumulators (the epilogue of one tile overlaps the next tile's
+  // MMAs) where they fit beside the metadata ring, else one.
+  static constexpr int ACC_BUFS = 2 * BNP + STAGES * T::META_COLS <= 512 ? 2 : 1;
+  static constexpr int META_COL0 = ACC_BUFS * BNP;   // after the accumulators
   static constexpr int TMEM_COLS = 512;
   static constexpr int CBUF_BYTES = 32 * 32 * 4;                     // one warp's 32 x 32 chunk of C (fp32 at most)
   static constexpr int C_BYTES = 4 * 2 * CBUF_BYTES;                  // 4 epilogue warps, double-buffered
@@ -76,13 +83,13 @@ struct PairConfig {
   static constexpr uint32_t IDESC = (1u << 2) | (1u << 4) | (T::FMT << 7) | (T::FMT << 10) |
                                     (static_cast<uint32_t>(BNP >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
   static_assert(BNP % 32 == 0 && BNP >= 64 && BNP <= 256, "N of the pair MMA; B halves of whole swizzle atoms");
-  static_assert(2 * BNP + STAGES * T::META_COLS <= TMEM_COLS, "tensor memory");
+  static_assert(ACC_BUFS * BNP + STAGES * T::META_COLS <= TMEM_COLS, "tensor memory");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
   static_assert((4 * STAGES + 5 + 8) * 8 + 8 + STAGES * 16 <= 512, "barrier region");
 };
 
 template <int DT, int BNP, int STAGES>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     spmm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmE,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
                     const __grid_constant__ CUtensorMap tmCc, const TcParams p) {
@@ -136,23 +143,21 @@ __global__ void __launch_bounds__(320, 1)
   // As in the one-CTA kernel: inputs are read after the dependency wait,
   // except fixed weights (ST24_SPMM_FIXED_A), whose first stages are loaded
   // before it; L2 is warmed with the weight tiles after those.
-  // Only the producer (B, after its preloads) and the epilogue warps (C, the
-  // workspace, the row scales) touch global memory; they wait for the
+  // Only the producers (after the weight preloads) and the epilogue warps (C,
+  // the workspace, the row scales) touch global memory; they wait for the
   // previous kernel, the MMA and metadata warps never need to.
   if (threadIdx.x == 0) grid_launch_dependents();
   if (warp >= 2 && warp <= 5) grid_dependency_wait();
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ weight producer
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmE);
-      tma_prefetch_desc(&tmB);
       const uint64_t stream_once = p.a_evict_first ? policy_evict_first() : policy_evict_last();
-      const uint64_t reuse = p.b_evict_first ? policy_evict_first() : policy_evict_last();
       uint32_t issued = 0, issued_parity = 0;   // per stage (bit s): a copy was issued, and its phase
-      // Arm stage s (the leader: for both CTAs' operand bytes) and load its
-      // metadata, then its A rows; B follows after the dependency wait.
+      // Arm stage s (the leader: for both CTAs' operand bytes, B included)
+      // and load its metadata, then its A rows.
       auto load_weights = [&](int s, int64_t kb, int32_t m0) {
         uint8_t* st = smem + s * Cfg::STAGE_BYTES;
         const uint32_t fb = smem_u32(&full_bar[s]), eb = smem_u32(&efull_bar[s]);
@@ -199,29 +204,23 @@ __global__ void __launch_bounds__(320, 1)
       bool ok = true;
       while (ok && have) {
         const int32_t m0 = static_cast<int32_t>((2 * mt64 + rank) * Cfg::BM);
-        const int32_t n0 = static_cast<int32_t>(nt64 * BNP + rank * Cfg::BH);
         if (p.prefetch_c && sg.kb1 == KI) tma_prefetch_l2_2d(&tmC, m0, static_cast<int32_t>(nt64 * BNP));
         for (int64_t kb = sg.kb0; kb < sg.kb1; ++kb, ++done) {
-          const uint32_t fb = smem_u32(&full_bar[stage]);
-          uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
           if (done >= preloaded) {
             if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) { ok = false; break; }
             load_weights(stage, kb, m0);
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
-          const int64_t kbb = (p.kb_wrap && kb >= p.kb_wrap) ? kb - p.kb_wrap : kb;
-          const int32_t kB = static_cast<int32_t>(kbb * T::BK);
-          tma_load_2d_pair(smem_u32(st + Cfg::A_BYTES), &tmB, kB, n0, fb, 0, reuse);
-          tma_load_2d_pair(smem_u32(st + Cfg::A_BYTES + Cfg::BH * 128), &tmB, kB + 128 / T::ES, n0, fb, 0, reuse);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         have = sch.next(sg);
         if (have) tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt64, nt64);
       }
       // No copy may still be landing when the CTA exits: the leader's full
-      // barrier counts both CTAs' operand bytes (the peer waits for the
-      // leader at the final cluster barrier), each CTA's metadata barrier its own.
+      // barrier counts both CTAs' operand bytes, B included (the peer waits
+      // for the leader at the final cluster barrier), each CTA's metadata
+      // barrier its own.
       for (int s = 0; s < STAGES; ++s)
         if ((issued >> s) & 1u) {
           const uint32_t par = (issued_parity >> s) & 1u;
@@ -285,7 +284,7 @@ __global__ void __launch_bounds__(320, 1)
         if (!ok) break;
         if (elect_one_lane()) tc_commit_pair(smem_u32(&tfull_bar[abuf]), kBoth);
         __syncwarp();
-        if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
+        if (++abuf == Cfg::ACC_BUFS) { abuf = 0; aphase ^= 1u; }
       }
       // Both CTAs learn when every pair MMA has completed (before TMEM is freed).
       if (elect_one_lane()) tc_commit_pair(smem_u32(drain_bar), kBoth);
@@ -293,6 +292,34 @@ __global__ void __launch_bounds__(320, 1)
       mbar_wait(smem_u32(drain_bar), 0, p.status);
     } else if (lane == 0) {
       mbar_wait(smem_u32(drain_bar), 0, p.status);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ B producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmB);
+      const uint64_t reuse = p.b_evict_first ? policy_evict_first() : policy_evict_last();
+      Schedule sch(KI, p.dp_tiles, p.sk_tiles, G, pair);
+      Segment sg;
+      grid_dependency_wait();
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      while (ok && sch.next(sg)) {
+        int64_t mt, nt;
+        tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
+        const int32_t n0 = static_cast<int32_t>(nt * BNP + rank * Cfg::BH);
+        for (int64_t kb = sg.kb0; kb < sg.kb1; ++kb) {
+          // the slot's previous operands are consumed (both producers wait on the same phase)
+          if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&full_bar[stage]);
+          uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
+          const int64_t kbb = (p.kb_wrap && kb >= p.kb_wrap) ? kb - p.kb_wrap : kb;
+          const int32_t kB = static_cast<int32_t>(kbb * T::BK);
+          tma_load_2d_pair(smem_u32(st + Cfg::A_BYTES), &tmB, kB, n0, fb, 0, reuse);
+          tma_load_2d_pair(smem_u32(st + Cfg::A_BYTES + Cfg::BH * 128), &tmB, kB + 128 / T::ES, n0, fb, 0, reuse);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
     }
   } else if (warp >= 6) {
     // ------------------------------------------------------------ metadata
@@ -491,7 +518,7 @@ __global__ void __launch_bounds__(320, 1)
           reduce_split_row<Cfg::BM, BNP, 8>(p, p.partials, sch, tile, 2, static_cast<int>(rank), c_lo, c_hi,
                                              32 * q + lane, m, n_base, f);
       }
-      if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
+      if (++abuf == Cfg::ACC_BUFS) { abuf = 0; aphase ^= 1u; }
     }
     if (lane == 0) bulk_wait_all();   // this warp's output stores have completed
   }

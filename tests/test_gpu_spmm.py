@@ -314,9 +314,12 @@ def test_prefill_bf16_sampled_mma_sp():
 
 # Few, long output tiles: the CTA pairs split them over K and finish them
 # through the workspace (the last contributor sums the partials); more tiles
-# run as whole tiles in data-parallel waves.  Both schedules, with beta.
+# run as whole tiles in data-parallel waves.  Both schedules, with beta, on
+# 224- and 128-column tiles with two accumulators and (e4m3, N = 449..512)
+# 256-column tiles with one.
 @pytest.mark.parametrize("ab", ["bf16", "e4m3"])
-@pytest.mark.parametrize("M,N,K", [(256, 200, 32768), (512, 448, 16384), (1024, 1000, 2048)])
+@pytest.mark.parametrize("M,N,K", [(256, 200, 32768), (512, 448, 16384), (1024, 1000, 2048), (1000, 500, 4096),
+                                   (256, 480, 65536)])
 def test_pair_schedules(ab, M, N, K):
     case = inputs.spmm_case(ab, "bf16", M, N, K, a_std=0.02 if ab == "e4m3" else 1.0, seed=M + N, beta=0.5)
     check_sampled(case, count=1024, kernel="tcgen05")
