@@ -182,7 +182,10 @@ __global__ void __launch_bounds__(480, 1)
     // ------------------------------------------------------------ dY producer
     if (lane == 0) {
       tma_prefetch_desc(&tmB);
-      const uint64_t keep = policy_evict_last();
+      // dY evict-first: each panel is read by the tiles of one wave, while the
+      // compressed weight is re-read by every panel and stays resident
+      // (11008x4096 at N = 4096: DRAM reads 282 -> 215 MB per launch).
+      const uint64_t keep = policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;

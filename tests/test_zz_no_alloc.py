@@ -78,10 +78,10 @@ def test_noalloc_matches_spmm_twice(case):
 
 
 def test_noalloc_rejects_more_than_its_scratch():
-    # N = 4096 on a 4352 x 4096 weight: its 17 x 19 tiles of 256 x 224 do not fill whole waves of
-    # CTA pairs, and the stream-K tail's partial tiles need ~35 MB
-    case = inputs.spmm_case("bf16", "bf16", 4352, 4096, 4096, a_std=0.02, seed=1)
-    assert st.st24_spmm_workspace_bytes("bf16", "bf16", 4352, 4096, 4096) > 16 << 20
+    # N = 4096 on a 512 x 32768 weight: 2 x 19 tiles of 256 x 224, fewer than the CTA pairs and
+    # long, so each is split two ways over K, and the 76 pairs' partial tiles need ~35 MB
+    case = inputs.spmm_case("bf16", "bf16", 512, 4096, 32768, a_std=0.02, seed=1)
+    assert st.st24_spmm_workspace_bytes("bf16", "bf16", 512, 4096, 32768) > 16 << 20
     values, meta, X, scale = prepare(case)
     Y = out_like(case)
     assert call_noalloc(case, values, meta, X, Y, scale) == 6   # ST24_ERR_WORKSPACE
