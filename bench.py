@@ -755,6 +755,7 @@ KERNEL_CASES = {
     "decode_narrow": "st24_spmm bf16 4096x4096, N = 16, 4 weights: 2 rounds of 4 launches of the narrow kernel",
     "prune_bf16": "st24_prune_compress and st24_prune_compress_nm2 (4:8) of a bf16 28672x8192 weight: twice each",
     "fp8_groups": "st24_spmm e4m3 28672x8192 at N = 512, 4096 and 8192 (the tensor-bound groups), one weight: two rounds",
+    "fp8_narrow": "st24_spmm e4m3 28672x8192 at N = 1 and 64 (the HBM-bound groups), one weight: two rounds",
     "decode_mix": "st24_spmm bf16 4096x4096 at N = 1, 16 and 32, one weight each: two rounds",
     "int8_mix": "st24_spmm int8 8192x8192 at N = 16 and 2048, row scales, bf16 out: two rounds",
     "demo_pair": "st24_spmm bf16 4096x4096, N = 4096: 3 launches",
@@ -805,6 +806,9 @@ def run_kernel_case(name):
     elif name == "fp8_groups":
         vm = compressed("e4m3", 28672, 8192)
         calls = [product("e4m3", 28672, 8192, n, 0.0, vm) for n in (512, 4096, 8192)] * 2
+    elif name == "fp8_narrow":
+        vm = compressed("e4m3", 28672, 8192)
+        calls = [product("e4m3", 28672, 8192, n, 0.0, vm) for n in (1, 64)] * 2
     elif name == "int8_mix":
         vm = compressed("s8", 8192, 8192)
         calls = [product("s8", 8192, 8192, n, 0.0, vm) for n in (16, 2048)] * 2
