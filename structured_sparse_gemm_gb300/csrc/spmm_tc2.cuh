@@ -18,8 +18,8 @@
 //    refills a stage when its own empty barrier (the MMA commit, multicast)
 //    says it is free.  Two issuing threads, because one thread issues tensor
 //    loads at a bounded rate (~90 cycles per box plus ~1 cycle per 117 bytes,
-//    measured): metadata, A and the two B boxes of a stage from one thread
-//    took ~800 cycles against ~450 of MMA work.
+//    measured by a load-only probe), which put the metadata, A and the two B
+//    boxes of a stage at ~800 cycles of issue against ~450 of MMA work.
 //  * warps 6-9, metadata: once this CTA's metadata has landed, shared memory
 //    -> this CTA's TMEM (as in the one-CTA kernel), then signal the leader
 //    CTA's meta barrier: the leader's warps arrive on it (4 arrivals, each
