@@ -511,7 +511,11 @@ st24_status launch_dt_impl(const SpmmArgs& a, const StreamKPlan& plan, const Dev
   constexpr bool k16 = TcTraits<DT>::ES == 2;
   if (plan.pair) {
     if (plan.bn == 128) return tc2::launch_pair<DT, 128, 5>(a, plan, dev, s);
-    if (plan.bn == 256) return tc2::launch_pair<DT, 256, 3>(a, plan, dev, s);
+    // 256-column tiles: 4 stages when beta = 0 (no C staging buffers;
+    // e4m3 28672x8192 at N = 512: 71.9 -> 66.8 us against 3 stages)
+    if (plan.bn == 256)
+      return a.beta == 0.0f ? tc2::launch_pair<DT, 256, 4, false>(a, plan, dev, s)
+                            : tc2::launch_pair<DT, 256, 3>(a, plan, dev, s);
     return tc2::launch_pair<DT, 224, 4>(a, plan, dev, s);
   }
   switch (plan.bn) {

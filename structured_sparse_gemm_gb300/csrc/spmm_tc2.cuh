@@ -56,7 +56,7 @@ __device__ __forceinline__ float staged_c(uint32_t at) {
 using tc::TcParams;
 using tc::TcTraits;
 
-template <int DT, int BNP_, int STAGES_>
+template <int DT, int BNP_, int STAGES_, bool CST = true>
 struct PairConfig {
   using T = TcTraits<DT>;
   static constexpr int BM = 128;                     // rows of A and D per CTA (M = 256 per pair)
@@ -76,7 +76,10 @@ struct PairConfig {
   static constexpr int META_COL0 = ACC_BUFS * BNP;   // after the accumulators
   static constexpr int TMEM_COLS = 512;
   static constexpr int CBUF_BYTES = 32 * 32 * 4;                     // one warp's 32 x 32 chunk of C (fp32 at most)
-  static constexpr int C_BYTES = 4 * 2 * CBUF_BYTES;                  // 4 epilogue warps, double-buffered
+  // 4 epilogue warps, double-buffered; none (CST false) when the shared
+  // memory goes to one more operand stage and the outputs leave by direct
+  // coalesced stores (beta = 0: no C to stage).
+  static constexpr int C_BYTES = CST ? 4 * 2 * CBUF_BYTES : 0;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + C_BYTES + 1024 + 512;   // + alignment, barriers, signal words
   static constexpr int CH = 32;                      // columns per tcgen05.ld
   // Instruction descriptor: sparse, fp32 accumulator, K-major A and B, N = BNP, M = 256.
@@ -88,12 +91,12 @@ struct PairConfig {
   static_assert((4 * STAGES + 5 + 8) * 8 + 8 + STAGES * 16 <= 512, "barrier region");
 };
 
-template <int DT, int BNP, int STAGES>
+template <int DT, int BNP, int STAGES, bool CST>
 __global__ void __launch_bounds__(352, 1)
     spmm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmE,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
                     const __grid_constant__ CUtensorMap tmCc, const TcParams p) {
-  using Cfg = PairConfig<DT, BNP, STAGES>;
+  using Cfg = PairConfig<DT, BNP, STAGES, CST>;
   using T = TcTraits<DT>;
   constexpr uint16_t kBoth = 0x3;
 
@@ -532,12 +535,12 @@ __global__ void __launch_bounds__(352, 1)
 }
 
 // Pairs that can be resident at once for this kernel (its clusters of 2).
-template <int DT, int BNP, int STAGES>
+template <int DT, int BNP, int STAGES, bool CST>
 int resident_pairs(int num_sms) {
-  using Cfg = PairConfig<DT, BNP, STAGES>;
+  using Cfg = PairConfig<DT, BNP, STAGES, CST>;
   static int pairs = 0;
   if (pairs == 0) {
-    auto kern = spmm_tc2_kernel<DT, BNP, STAGES>;
+    auto kern = spmm_tc2_kernel<DT, BNP, STAGES, CST>;
     int n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
@@ -558,9 +561,9 @@ int resident_pairs(int num_sms) {
   return pairs;
 }
 
-template <int DT, int BNP, int STAGES>
+template <int DT, int BNP, int STAGES, bool CST = true>
 st24_status launch_pair(const SpmmArgs& a, const StreamKPlan& plan, const DeviceInfo& dev, cudaStream_t stream) {
-  using Cfg = PairConfig<DT, BNP, STAGES>;
+  using Cfg = PairConfig<DT, BNP, STAGES, CST>;
   using T = TcTraits<DT>;
   const CUtensorMapDataType ty = T::ES == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   CUtensorMap tmA, tmE, tmB;
@@ -586,7 +589,7 @@ st24_status launch_pair(const SpmmArgs& a, const StreamKPlan& plan, const Device
   if (!c_map) tmCc = tmA;        // unused
   if (!c_prefetch) tmC = tmA;    // unused
   TcParams p{};
-  p.c_tma = c_map ? 1 : 0;
+  p.c_tma = (c_map && CST) ? 1 : 0;
   p.prefetch_c = c_prefetch ? 1 : 0;
   p.M = a.M; p.N = a.N; p.K = a.K;
   p.kb_wrap = (a.Kb && a.Kb != a.K) ? a.Kb / T::BK : 0;
@@ -615,8 +618,8 @@ st24_status launch_pair(const SpmmArgs& a, const StreamKPlan& plan, const Device
                                                           2 * static_cast<size_t>(plan.grid) * plan.partial_bytes)
                              : nullptr;
   p.status = dev.status;
-  auto kern = spmm_tc2_kernel<DT, BNP, STAGES>;
-  resident_pairs<DT, BNP, STAGES>(dev.num_sms);   // sets the kernel's shared-memory attribute once
+  auto kern = spmm_tc2_kernel<DT, BNP, STAGES, CST>;
+  resident_pairs<DT, BNP, STAGES, CST>(dev.num_sms);   // sets the kernel's shared-memory attribute once
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * plan.grid));
   cfg.blockDim = dim3(Cfg::THREADS);

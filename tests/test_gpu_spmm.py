@@ -323,3 +323,11 @@ def test_prefill_bf16_sampled_mma_sp():
 def test_pair_schedules(ab, M, N, K):
     case = inputs.spmm_case(ab, "bf16", M, N, K, a_std=0.02 if ab == "e4m3" else 1.0, seed=M + N, beta=0.5)
     check_sampled(case, count=1024, kernel="tcgen05")
+
+
+# e4m3 256-column tiles with beta = 0 run with one more stage and no C
+# staging (outputs by direct stores): whole tiles and tiles split over K.
+@pytest.mark.parametrize("M,N,K", [(1000, 500, 4096), (256, 480, 65536)])
+def test_wide_tiles_beta0(M, N, K):
+    case = inputs.spmm_case("e4m3", "bf16", M, N, K, a_std=0.02, seed=M + N + K + 1)
+    check_sampled(case, count=1024, kernel="tcgen05")
